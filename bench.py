@@ -1,0 +1,402 @@
+#!/usr/bin/env python3
+"""Fused linear cross-entropy forward+backward throughput on GB300.
+
+One step = one flce_fwd_bwd call (logits GEMM + online LSE, merge, then per
+vocabulary chunk the dZ recompute, dW and dX GEMMs, and the dX conversion)
+over one batch of N tokens of the chosen synthetic workload.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line on rank 0.  ``value`` is tokens/s over all ranks with
+inputs resident in HBM; ``e2e`` is the same metric with the inputs copied
+from pinned host memory and the outputs (loss, lse, dX, dW) copied back inside
+the timed region.  With N > 1 every rank runs its own batch (weak scaling, no
+collective on the data path).  ``--impl reference`` times the fp64 CPU oracle
+on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused fwd+bwd tokens/s and TFLOP/s (% of BF16 tensor roofline), 1×GB300"
+DEFAULT_WORKLOAD = "llama3_n8192"
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--vocab-chunk", type=int, default=0,
+                    help="vocabulary columns per backward chunk (0 = automatic)")
+    ap.add_argument("--cpu-baseline-rows", type=int, default=1024,
+                    help="token rows of the oracle sample timed on the host (0 = skip)")
+    ap.add_argument("--reference-rows", type=int, default=128,
+                    help="token rows per oracle step of --impl reference")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        return {"bf16_burst": float(d["bf16_tflops"]),
+                "bf16_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"bf16_burst": 1900.0, "bf16_sustained": 1700.0, "hbm_gbs": 6800.0,
+                "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------
+# Clock sampling during the timed region
+# ----------------------------------------------------------------------------
+CLOCK_FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+                "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                "clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, gpu_index: str):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", gpu_index], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) != 7:
+                    continue
+                try:
+                    rows.append((float(parts[0]), float(parts[1]), parts[2], parts[3:]))
+                except ValueError:
+                    continue
+        if not rows:
+            return None
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3]) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows), "samples": len(rows),
+                "reasons": reasons}
+
+
+# ----------------------------------------------------------------------------
+# Reference arm: the fp64 oracle on the host cores
+# ----------------------------------------------------------------------------
+def oracle_sample(wl, rows: int):
+    """The oracle's fused forward+backward on the first ``rows`` tokens."""
+    from oracle import flce_oracle as O
+    r = min(rows, wl.N)
+    t0 = time.perf_counter()
+    O.fwd_bwd(wl.x[:r], wl.w, wl.labels[:r], wl.spec.ignore_index, wl.spec.smoothing,
+              wl.spec.reduction)
+    return r, time.perf_counter() - t0
+
+
+def run_reference(args, rank: int):
+    from linear_cross_entropy_logit_gb300 import inputs as I
+    if rank != 0:
+        return
+    spec = I.CONFIGS[args.workload]
+    wl = I.make_workload(spec, seed=args.seed)
+    for _ in range(args.warmup):
+        oracle_sample(wl, args.reference_rows)
+    total_rows, total_s = 0, 0.0
+    for _ in range(args.steps):
+        r, dt = oracle_sample(wl, args.reference_rows)
+        total_rows += r
+        total_s += dt
+    value = total_rows / total_s
+    cores = host_cores()
+    sample = (f"first {min(args.reference_rows, wl.N)} of {wl.N} tokens per step, full V and H, "
+              f"fp64 oracle forward+backward (numpy float64 matmul)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(spec, None),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(spec, chunk):
+    cfg = {"workload": spec.name, "N": spec.N, "H": spec.H, "V": spec.V,
+           "inputs": f"X {spec.dtype} N(0,{spec.x_std}^2)"
+                     + (" RMS-normed rows" if spec.x_rms_rows else "")
+                     + f", W {spec.dtype} N(0,{spec.w_std}^2)"
+                     + (f" with {spec.n_scaled_w_rows} rows x{spec.w_row_scale:g}"
+                        if spec.n_scaled_w_rows else "")
+                     + f", labels {spec.labels}",
+           "ignored_tokens": spec.n_ignore, "ignore_index": spec.ignore_index,
+           "smoothing": spec.smoothing, "reduction": spec.reduction}
+    if chunk is not None:
+        cfg["vocab_chunk"] = chunk
+    return cfg
+
+
+# ----------------------------------------------------------------------------
+# Our arm
+# ----------------------------------------------------------------------------
+def run_ours(args, rank: int, world: int, local_rank: int):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from linear_cross_entropy_logit_gb300 import build as libbuild
+    from linear_cross_entropy_logit_gb300 import inputs as I
+
+    if rank == 0:
+        libbuild.build()
+    if world > 1:
+        dist.barrier()
+    from linear_cross_entropy_logit_gb300 import binding as B
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    spec = I.CONFIGS[args.workload]
+    wl = I.make_workload(spec, seed=args.seed + rank)
+    N, H, V = spec.N, spec.H, spec.V
+    B.flce_set_vocab_chunk(args.vocab_chunk)
+    chunk = B.flce_vocab_chunk(N, V)
+
+    def host_tensor(a):
+        if spec.dtype == "bf16":
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(a))
+
+    Xh, Wh = host_tensor(wl.x), host_tensor(wl.w)
+    yh = torch.from_numpy(wl.labels)
+    X, W, y = Xh.to(dev), Wh.to(dev), yh.to(dev)
+    dt = B.FLCE_BF16 if spec.dtype == "bf16" else B.FLCE_FP32
+    ws = B.workspace(N, H, V, dt, B.MODE_FWD_BWD, dev)
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    lse = torch.empty(N, dtype=torch.float32, device=dev)
+    nv = torch.empty(1, dtype=torch.int32, device=dev)
+    dX = torch.empty_like(X)
+    dW = torch.empty(V, H, dtype=torch.float32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    base_mem = torch.cuda.memory_allocated(dev)
+
+    def step():
+        B.flce_fwd_bwd(X, W, y, spec.ignore_index, spec.smoothing, spec.reduction, loss=loss,
+                       lse=lse, valid_count=nv, dX=dX, dW=dW, workspace_buf=ws, err_word=err,
+                       stream=stream)
+        return B.last_launch_count()
+
+    for _ in range(max(args.warmup, 0)):
+        step()
+    torch.cuda.synchronize(dev)
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item())} after warm-up")
+
+    gpu_index = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[local_rank] \
+        if os.environ.get("CUDA_VISIBLE_DEVICES") else str(local_rank)
+    B.flce_profile_reset()
+    B.flce_profile_enable(True)
+    sampler = ClockSampler(gpu_index) if rank == 0 else None
+    time.sleep(0.2 if sampler else 0.0)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    wall0 = time.perf_counter()
+    ev0.record(stream)
+    launches = 0
+    for _ in range(args.steps):
+        launches += step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop() if sampler else None
+    B.flce_profile_enable(False)
+    prof = B.flce_profile_read()
+    ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item())} in the timed region")
+    ms_per_step = ms / args.steps
+    tokens_per_s = world * N * args.steps / (ms / 1e3)
+
+    # --- end-to-end through the C ABI with host buffers --------------------
+    e2e = None
+    if not args.no_e2e:
+        Xp, Wp, yp = Xh.pin_memory(), Wh.pin_memory(), yh.pin_memory()
+        loss_h = torch.empty(1, dtype=torch.float32).pin_memory()
+        lse_h = torch.empty(N, dtype=torch.float32).pin_memory()
+        dX_h = torch.empty(dX.shape, dtype=dX.dtype).pin_memory()
+        dW_h = torch.empty(dW.shape, dtype=torch.float32).pin_memory()
+        h2d = Xp.numel() * Xp.element_size() + Wp.numel() * Wp.element_size() + yp.numel() * 8
+        d2h = 4 + 4 * N + dX_h.numel() * dX_h.element_size() + dW_h.numel() * 4
+
+        def e2e_step():
+            X.copy_(Xp, non_blocking=True)
+            W.copy_(Wp, non_blocking=True)
+            y.copy_(yp, non_blocking=True)
+            step()
+            loss_h.copy_(loss, non_blocking=True)
+            lse_h.copy_(lse, non_blocking=True)
+            dX_h.copy_(dX, non_blocking=True)
+            dW_h.copy_(dW, non_blocking=True)
+
+        for _ in range(max(args.warmup, 1)):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ems = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([ems], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": world * N * args.steps / (ems / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": ems / args.steps}
+
+    if rank != 0:
+        return
+
+    pk = peaks()
+    flops_step = 8.0 * N * V * H
+    tflops = flops_step / (ms_per_step / 1e3) / 1e12
+    # algorithmic bytes of one step: X, W read; dX, dW written; labels, lse
+    elem = 2 if spec.dtype == "bf16" else 4
+    bytes_step = N * H * elem * 2 + V * H * elem + V * H * 4 + N * 8 + N * 4
+    t_tensor = flops_step / (pk["bf16_sustained"] * 1e12)
+    t_hbm = bytes_step / (pk["hbm_gbs"] * 1e9)
+    step_frac = max(t_tensor, t_hbm) / (ms_per_step / 1e3)
+
+    # dominant kernel: largest share of the profiled device time
+    kinds = {}
+    flops_kind = 2.0 * N * V * H  # each kind performs one 2NVH contraction per step
+    total_prof_ms = sum(v[0] for v in prof.values()) or 1.0
+    for name, (kms, n) in prof.items():
+        if n == 0:
+            continue
+        kinds[name] = {"launches": n, "ms_total": kms, "ms_per_launch": kms / n,
+                       "share_of_gemm_time": kms / total_prof_ms,
+                       "tflops": flops_kind * args.steps / (kms / 1e3) / 1e12}
+    dom = max(kinds, key=lambda k: kinds[k]["ms_total"]) if kinds else None
+    roofline = None
+    if dom:
+        ach = kinds[dom]["tflops"]
+        roofline = {"bound": "tensor", "achieved": ach, "peak": pk["bf16_sustained"],
+                    "unit": "TFLOP/s", "frac": ach / pk["bf16_sustained"], "traffic": None,
+                    "kernel": dom,
+                    "peak_source": f"{pk['source']} bf16 sustained (MEASURED_PEAKS.json)"
+                    if pk["source"] == "measured" else "fallback bf16 sustained"}
+
+    cpu = None
+    if args.cpu_baseline_rows > 0 and world == 1:
+        r, secs = oracle_sample(wl, args.cpu_baseline_rows)
+        cpu = {"value": r / secs, "unit": "tokens/s", "cores": host_cores(), "kind": "oracle",
+               "sample": f"first {r} of {N} tokens, full V={V} and H={H}, fp64 oracle "
+                         f"forward+backward (numpy float64 matmul), {secs:.1f} s"}
+
+    extra = {"workspace_bytes": ws.numel(),
+             "workspace_vs_nxv_bf16": ws.numel() / (N * V * 2),
+             "dz_chunk_bytes": N * chunk * 2,
+             "peak_extra_device_bytes": torch.cuda.max_memory_allocated(dev) - base_mem}
+    line = {
+        "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": spec.dtype, "data": "synthetic",
+        "config": dict(workload_config(spec, chunk),
+                       l2="inputs larger than L2 (W alone is %.2f GB)" % (V * H * elem / 1e9),
+                       parallelism=f"replicas x{world} (each rank its own batch, no collective)"),
+        "tflops": tflops,
+        "step_roofline": {"bound": "tensor" if t_tensor >= t_hbm else "hbm",
+                          "frac": step_frac, "flops": flops_step, "bytes": bytes_step,
+                          "peak_tflops": pk["bf16_sustained"], "peak_source": pk["source"]},
+        "roofline": roofline,
+        "kernels": kinds,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "wall_s_timed": wall,
+        "memory": extra,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    if args.warmup < 3:
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    import torch.distributed as dist
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,162 @@
+/*
+ * flce.h -- fused linear cross-entropy on one GB300 (sm_103a): C ABI.
+ *
+ * The library computes, for hidden states X (N x H), an unembedding matrix W
+ * (V x H) and integer targets y (N):
+ *
+ *   Z      = X W^T                       logits, never stored (N x V)
+ *   lse_i  = m_i + log sum_j exp(z_ij - m_i),  m_i = max_j z_ij
+ *   l_i    = valid_i * (lse_i - (1-eps) z_{i,y_i} - (eps/V) sum_j z_ij)
+ *   loss   = sum_i l_i / N_valid  (mean)   or   sum_i l_i  (sum)
+ *   dZ_ij  = c * valid_i * (exp(z_ij - lse_i) - (1-eps) 1[j = y_i] - eps/V)
+ *   dX     = dZ W,   dW = dZ^T X  (dW += when accumulating)
+ *
+ * with valid_i = (y_i != ignore_index), N_valid = sum_i valid_i and
+ * c = grad_loss / N_valid (mean; 0 when N_valid = 0) or c = grad_loss (sum).
+ *
+ * Sources (page title, section):
+ *   "Chunked and Fused Cross-Entropy: How Online Logit Tiling Slashes
+ *    Large-Vocabulary VRAM Bottlenecks in LLM Training" -- the projection and
+ *    loss equations ("The Vocabulary Memory Wall in Modern LLMs") and steps
+ *    1-4 of "Mathematical Mechanics of Chunked Online Cross-Entropy"; label
+ *    -100 masking and label smoothing ("Numerical Considerations and
+ *    Practical Trade-Offs", items 2-3).
+ *   "Cut Cross-Entropy: Memory-Efficient Large-Vocab LLM Guide" -- the call
+ *    linear_cross_entropy(h, W, labels, ignore_index=-100) and the chunked
+ *    reference's mean over max(valid_token_count, 1).
+ *   "Fused cross-entropy -- the memory kernel" -- dlogits = (p - y)/N,
+ *    "Trick 1" (online softmax) and "Trick 2" (fuse the lm-head matmul).
+ * Label smoothing follows PyTorch's convention (eps/V of the mass on every
+ * class, the target keeps 1 - eps + eps/V); the pages name the term without
+ * a formula.
+ *
+ * Conventions for every entry point
+ *   - All tensor pointers are DEVICE pointers, row-major and contiguous:
+ *     X is N x H, W is V x H (the nn.Linear weight layout), labels is N int64,
+ *     dX is N x H, dW is V x H float32, lse is N float32.
+ *   - X, W and dX use `dtype` (bf16 or fp32); X, W, dX, dW must be 16-byte
+ *     aligned and H must be a multiple of 8 (rows are fetched by TMA).
+ *   - fp32 inputs are rounded to bf16 once (in the workspace) and multiplied
+ *     on the bf16 tensor cores with fp32 accumulation; dX is then fp32.
+ *   - The caller owns every buffer, the workspace included.  The library
+ *     allocates no device memory and never materialises an N x V tensor: its
+ *     largest region is an N x Cv bf16 gradient chunk with Cv <= V/2.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream) and never synchronise the host.
+ *   - Argument errors are reported synchronously by the return value and
+ *     launch nothing.  Data errors are reported through *err_word (device
+ *     int32 the caller zeroes beforehand; the first error code wins and stays
+ *     set): FLCE_ERR_LABEL for a label outside [0, V) that is not
+ *     ignore_index (that row then counts as ignored), FLCE_ERR_TIMEOUT if a
+ *     kernel's bounded wait expired (outputs are then undefined).  Read it
+ *     after synchronising the stream.
+ *   - N = 0 is allowed (loss 0, no valid tokens, dW zeroed unless
+ *     accumulating).  ignore_index may be any value; a value inside [0, V)
+ *     masks that class.
+ */
+#ifndef FLCE_H_
+#define FLCE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FLCE_OK = 0,
+  FLCE_ERR_ARG = 1,          /* bad pointer, size, alignment or option      */
+  FLCE_ERR_UNSUPPORTED = 2,  /* no sm_100-family device, or a size limit     */
+  FLCE_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required  */
+  FLCE_ERR_LABEL = 4,        /* (err_word only) label outside [0, V)        */
+  FLCE_ERR_TIMEOUT = 5,      /* (err_word only) a bounded device wait expired */
+  FLCE_ERR_CUDA = 6          /* a CUDA runtime/driver call failed           */
+} flce_status;
+
+typedef enum { FLCE_BF16 = 0, FLCE_FP32 = 1 } flce_dtype;
+typedef enum { FLCE_MEAN = 0, FLCE_SUM = 1 } flce_reduction;
+typedef enum { FLCE_MODE_FWD = 1, FLCE_MODE_BWD = 2, FLCE_MODE_FWD_BWD = 3 } flce_mode;
+
+/* Bytes of workspace one call of `mode` needs for this shape (0 on invalid
+ * arguments).  Pure host arithmetic: needs no GPU.  The layout depends only on
+ * (N, H, V, dtype, mode) and the vocabulary chunk setting below. */
+size_t flce_workspace_size(int64_t N, int64_t H, int64_t V, flce_dtype dtype, int mode);
+
+/* Vocabulary columns per backward chunk (Cv): the gradient scratch is N x Cv
+ * bf16.  0 (the default) picks the largest multiple of 256 whose scratch fits
+ * in 256 MiB, clamped to [256, V/2].  A non-zero value is rounded up to a
+ * multiple of 256.  Process-wide; set it before sizing workspaces. */
+flce_status flce_set_vocab_chunk(int64_t cols);
+int64_t flce_vocab_chunk(int64_t N, int64_t V);
+
+/* Forward ("Mathematical Mechanics of Chunked Online Cross-Entropy", steps
+ * 1-2): loss (device float, 1), lse (device float, N, every row including
+ * ignored ones), valid_count (device int32, 1: N_valid).  workspace: device,
+ * 256-byte aligned, at least flce_workspace_size(..., FLCE_MODE_FWD). */
+flce_status flce_forward(const void* X, const void* W, const int64_t* labels, int64_t N,
+                         int64_t H, int64_t V, int64_t ignore_index, float smoothing,
+                         flce_dtype dtype, flce_reduction reduction, float* loss, float* lse,
+                         int32_t* valid_count, void* workspace, size_t ws_bytes,
+                         int32_t* err_word, void* stream);
+
+/* Backward (steps 3-4): recomputes the logits tile by tile from X, W and the
+ * forward's lse, forms dZ in bf16 and writes dX (N x H, dtype, overwritten)
+ * and dW (V x H fp32; overwritten, or added to when accumulate_dW != 0).
+ * valid_count: the forward's N_valid (device int32) -- a data-parallel caller
+ * may pass the global count.  grad_loss: device float (upstream gradient of
+ * the loss) or NULL for 1.  workspace: >= flce_workspace_size(..., FLCE_MODE_BWD). */
+flce_status flce_backward(const void* X, const void* W, const int64_t* labels, int64_t N,
+                          int64_t H, int64_t V, int64_t ignore_index, float smoothing,
+                          flce_dtype dtype, flce_reduction reduction, const float* lse,
+                          const int32_t* valid_count, const float* grad_loss, void* dX,
+                          float* dW, int accumulate_dW, void* workspace, size_t ws_bytes,
+                          int32_t* err_word, void* stream);
+
+/* Forward then backward in one call (the fused training step of the pages'
+ * "Trick 2"): loss, lse, valid_count, dX, dW as above.
+ * workspace: >= flce_workspace_size(..., FLCE_MODE_FWD_BWD). */
+flce_status flce_fwd_bwd(const void* X, const void* W, const int64_t* labels, int64_t N,
+                         int64_t H, int64_t V, int64_t ignore_index, float smoothing,
+                         flce_dtype dtype, flce_reduction reduction, const float* grad_loss,
+                         float* loss, float* lse, int32_t* valid_count, void* dX, float* dW,
+                         int accumulate_dW, void* workspace, size_t ws_bytes, int32_t* err_word,
+                         void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* flce_status_string(flce_status s);
+
+/* Text of the last CUDA error this thread saw inside the library ("" if none). */
+const char* flce_last_cuda_error(void);
+
+/* Number of kernels the last flce_forward / flce_backward / flce_fwd_bwd call
+ * on this thread enqueued. */
+int flce_last_launch_count(void);
+
+/* Optional per-kernel timing.  While enabled (per host thread), every GEMM
+ * launch of the calls above is bracketed by two CUDA events recorded on the
+ * caller's stream.  flce_profile_read synchronises the recorded events and
+ * returns the accumulated device time and launch count of one kernel kind:
+ * 0 forward logits + online LSE, 1 dZ recompute, 2 dW GEMM, 3 dX GEMM.
+ * flce_profile_reset clears the totals. */
+flce_status flce_profile_enable(int on);
+flce_status flce_profile_read(int kind, double* total_ms, int* launches);
+void flce_profile_reset(void);
+
+/* ABI version of this header (major * 100 + minor). */
+int flce_abi_version(void);
+
+/* TEST-ONLY: the library's tcgen05 GEMM core without a loss epilogue.
+ * D (M x Nn fp32, device, row-major) = A * B^T, or += when accumulate != 0,
+ * where A is M x K (a_mn = 0: stored M x K row-major) or stored K x M
+ * (a_mn = 1), and B is Nn x K (b_mn = 0: stored Nn x K) or stored K x Nn
+ * (b_mn = 1); A and B are bf16.  Exercises the K-major and MN-major operand
+ * descriptors in isolation; no part of the loss path calls it. */
+flce_status flce_debug_gemm(const void* A, const void* B, float* D, int64_t M, int64_t Nn,
+                            int64_t K, int a_mn, int b_mn, int accumulate, int32_t* err_word,
+                            void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FLCE_H_ */

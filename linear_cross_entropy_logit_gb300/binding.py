@@ -1,0 +1,294 @@
+"""Thin ctypes binding of ``libflce.so`` (include/flce.h).
+
+Argument marshalling only: every step of the forward and backward runs in the
+library's CUDA kernels.  PyTorch provides device memory and the stream.  If the
+library is missing, ``lib()`` raises instead of falling back to anything.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libflce.so")
+
+FLCE_OK = 0
+FLCE_ERR_ARG = 1
+FLCE_ERR_UNSUPPORTED = 2
+FLCE_ERR_WORKSPACE = 3
+FLCE_ERR_LABEL = 4
+FLCE_ERR_TIMEOUT = 5
+FLCE_ERR_CUDA = 6
+
+FLCE_BF16 = 0
+FLCE_FP32 = 1
+FLCE_MEAN = 0
+FLCE_SUM = 1
+MODE_FWD = 1
+MODE_BWD = 2
+MODE_FWD_BWD = 3
+
+EXPORTED = (
+    "flce_workspace_size", "flce_set_vocab_chunk", "flce_vocab_chunk", "flce_forward",
+    "flce_backward", "flce_fwd_bwd", "flce_status_string", "flce_last_cuda_error",
+    "flce_last_launch_count", "flce_abi_version", "flce_debug_gemm", "flce_profile_enable",
+    "flce_profile_read", "flce_profile_reset",
+)
+
+PROFILE_KINDS = ("fwd_logits_lse", "bwd_dz_recompute", "bwd_dw_gemm", "bwd_dx_gemm")
+
+_lib = None
+
+
+class FlceError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        detail = ""
+        if status == FLCE_ERR_CUDA:
+            detail = " (" + lib().flce_last_cuda_error().decode() + ")"
+        super().__init__(f"{what}: {lib().flce_status_string(status).decode()}{detail}")
+
+
+def lib() -> ctypes.CDLL:
+    """Load the library (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"{LIB_PATH} is missing: build it with "
+            "`python -m linear_cross_entropy_logit_gb300.build` (needs nvcc)")
+    L = ctypes.CDLL(LIB_PATH)
+    P, I64, I32, F32, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    L.flce_workspace_size.argtypes = [I64, I64, I64, I32, I32]
+    L.flce_workspace_size.restype = SZ
+    L.flce_set_vocab_chunk.argtypes = [I64]
+    L.flce_set_vocab_chunk.restype = I32
+    L.flce_vocab_chunk.argtypes = [I64, I64]
+    L.flce_vocab_chunk.restype = I64
+    L.flce_forward.argtypes = [P, P, P, I64, I64, I64, I64, F32, I32, I32, P, P, P, P, SZ, P, P]
+    L.flce_forward.restype = I32
+    L.flce_backward.argtypes = [P, P, P, I64, I64, I64, I64, F32, I32, I32, P, P, P, P, P, I32,
+                                P, SZ, P, P]
+    L.flce_backward.restype = I32
+    L.flce_fwd_bwd.argtypes = [P, P, P, I64, I64, I64, I64, F32, I32, I32, P, P, P, P, P, P, I32,
+                               P, SZ, P, P]
+    L.flce_fwd_bwd.restype = I32
+    L.flce_status_string.argtypes = [I32]
+    L.flce_status_string.restype = ctypes.c_char_p
+    L.flce_last_cuda_error.argtypes = []
+    L.flce_last_cuda_error.restype = ctypes.c_char_p
+    L.flce_last_launch_count.argtypes = []
+    L.flce_last_launch_count.restype = I32
+    L.flce_abi_version.argtypes = []
+    L.flce_abi_version.restype = I32
+    L.flce_debug_gemm.argtypes = [P, P, P, I64, I64, I64, I32, I32, I32, P, P]
+    L.flce_debug_gemm.restype = I32
+    L.flce_profile_enable.argtypes = [I32]
+    L.flce_profile_enable.restype = I32
+    L.flce_profile_read.argtypes = [I32, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(I32)]
+    L.flce_profile_read.restype = I32
+    L.flce_profile_reset.argtypes = []
+    L.flce_profile_reset.restype = None
+    _lib = L
+    return L
+
+
+def _check(status: int, what: str) -> None:
+    if status != FLCE_OK:
+        raise FlceError(status, what)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return FLCE_BF16
+    if t.dtype == torch.float32:
+        return FLCE_FP32
+    raise TypeError(f"X and W must be bfloat16 or float32, got {t.dtype}")
+
+
+def _red_code(reduction: str) -> int:
+    if reduction == "mean":
+        return FLCE_MEAN
+    if reduction == "sum":
+        return FLCE_SUM
+    raise ValueError(f"reduction must be 'mean' or 'sum', got {reduction!r}")
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check_inputs(X, W, labels):
+    for name, t in (("X", X), ("W", W), ("labels", labels)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if X.dtype != W.dtype:
+        raise TypeError("X and W must have the same dtype")
+    if labels.dtype != torch.int64:
+        raise TypeError("labels must be int64")
+    N, H = X.shape
+    V, H2 = W.shape
+    if H2 != H or labels.shape != (N,):
+        raise ValueError(f"shape mismatch: X {tuple(X.shape)}, W {tuple(W.shape)}, labels {tuple(labels.shape)}")
+    return N, H, V
+
+
+def flce_workspace_size(N: int, H: int, V: int, dtype: int = FLCE_BF16, mode: int = MODE_FWD_BWD) -> int:
+    return int(lib().flce_workspace_size(N, H, V, dtype, mode))
+
+
+def flce_set_vocab_chunk(cols: int) -> None:
+    _check(lib().flce_set_vocab_chunk(cols), "flce_set_vocab_chunk")
+
+
+def flce_vocab_chunk(N: int, V: int) -> int:
+    return int(lib().flce_vocab_chunk(N, V))
+
+
+def workspace(N: int, H: int, V: int, dtype: int, mode: int, device) -> torch.Tensor:
+    """A workspace of the required size (torch-allocated, 256-byte aligned)."""
+    n = max(flce_workspace_size(N, H, V, dtype, mode), 256)
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def new_err_word(device) -> torch.Tensor:
+    return torch.zeros(1, dtype=torch.int32, device=device)
+
+
+def flce_forward(X, W, labels, ignore_index: int = -100, smoothing: float = 0.0,
+                 reduction: str = "mean", *, loss=None, lse=None, valid_count=None,
+                 workspace_buf=None, err_word=None, stream=None):
+    """Returns (loss[1] fp32, lse[N] fp32, valid_count[1] int32, err_word[1] int32)."""
+    N, H, V = _check_inputs(X, W, labels)
+    dev = X.device
+    dt = _dtype_code(X)
+    loss = torch.empty(1, dtype=torch.float32, device=dev) if loss is None else loss
+    lse = torch.empty(N, dtype=torch.float32, device=dev) if lse is None else lse
+    valid_count = torch.empty(1, dtype=torch.int32, device=dev) if valid_count is None else valid_count
+    ws = workspace(N, H, V, dt, MODE_FWD, dev) if workspace_buf is None else workspace_buf
+    err_word = new_err_word(dev) if err_word is None else err_word
+    st = lib().flce_forward(_ptr(X), _ptr(W), _ptr(labels), N, H, V, ignore_index, smoothing, dt,
+                            _red_code(reduction), _ptr(loss), _ptr(lse), _ptr(valid_count),
+                            _ptr(ws), ws.numel(), _ptr(err_word), _stream(stream))
+    _check(st, "flce_forward")
+    return loss, lse, valid_count, err_word
+
+
+def flce_backward(X, W, labels, lse, valid_count, ignore_index: int = -100,
+                  smoothing: float = 0.0, reduction: str = "mean", *, grad_loss=None,
+                  dX=None, dW=None, accumulate_dW: bool = False, workspace_buf=None,
+                  err_word=None, stream=None):
+    """Returns (dX [N, H] in X's dtype, dW [V, H] fp32, err_word)."""
+    N, H, V = _check_inputs(X, W, labels)
+    dev = X.device
+    dt = _dtype_code(X)
+    dX = torch.empty_like(X) if dX is None else dX
+    if dW is None:
+        if accumulate_dW:
+            raise ValueError("accumulate_dW needs an existing dW")
+        dW = torch.empty(V, H, dtype=torch.float32, device=dev)
+    ws = workspace(N, H, V, dt, MODE_BWD, dev) if workspace_buf is None else workspace_buf
+    err_word = new_err_word(dev) if err_word is None else err_word
+    st = lib().flce_backward(_ptr(X), _ptr(W), _ptr(labels), N, H, V, ignore_index, smoothing, dt,
+                             _red_code(reduction), _ptr(lse), _ptr(valid_count), _ptr(grad_loss),
+                             _ptr(dX), _ptr(dW), int(bool(accumulate_dW)), _ptr(ws), ws.numel(),
+                             _ptr(err_word), _stream(stream))
+    _check(st, "flce_backward")
+    return dX, dW, err_word
+
+
+def flce_fwd_bwd(X, W, labels, ignore_index: int = -100, smoothing: float = 0.0,
+                 reduction: str = "mean", *, grad_loss=None, loss=None, lse=None,
+                 valid_count=None, dX=None, dW=None, accumulate_dW: bool = False,
+                 workspace_buf=None, err_word=None, stream=None):
+    """Returns (loss, lse, valid_count, dX, dW, err_word)."""
+    N, H, V = _check_inputs(X, W, labels)
+    dev = X.device
+    dt = _dtype_code(X)
+    loss = torch.empty(1, dtype=torch.float32, device=dev) if loss is None else loss
+    lse = torch.empty(N, dtype=torch.float32, device=dev) if lse is None else lse
+    valid_count = torch.empty(1, dtype=torch.int32, device=dev) if valid_count is None else valid_count
+    dX = torch.empty_like(X) if dX is None else dX
+    if dW is None:
+        if accumulate_dW:
+            raise ValueError("accumulate_dW needs an existing dW")
+        dW = torch.empty(V, H, dtype=torch.float32, device=dev)
+    ws = workspace(N, H, V, dt, MODE_FWD_BWD, dev) if workspace_buf is None else workspace_buf
+    err_word = new_err_word(dev) if err_word is None else err_word
+    st = lib().flce_fwd_bwd(_ptr(X), _ptr(W), _ptr(labels), N, H, V, ignore_index, smoothing, dt,
+                            _red_code(reduction), _ptr(grad_loss), _ptr(loss), _ptr(lse),
+                            _ptr(valid_count), _ptr(dX), _ptr(dW), int(bool(accumulate_dW)),
+                            _ptr(ws), ws.numel(), _ptr(err_word), _stream(stream))
+    _check(st, "flce_fwd_bwd")
+    return loss, lse, valid_count, dX, dW, err_word
+
+
+def flce_debug_gemm(A, B, M: int, Nn: int, K: int, a_mn: bool, b_mn: bool, D=None,
+                    accumulate: bool = False, err_word=None, stream=None):
+    """Test-only: D (M x Nn fp32) = A B^T through the tcgen05 GEMM core."""
+    dev = A.device
+    D = torch.empty(M, Nn, dtype=torch.float32, device=dev) if D is None else D
+    err_word = new_err_word(dev) if err_word is None else err_word
+    st = lib().flce_debug_gemm(_ptr(A), _ptr(B), _ptr(D), M, Nn, K, int(a_mn), int(b_mn),
+                               int(accumulate), _ptr(err_word), _stream(stream))
+    _check(st, "flce_debug_gemm")
+    return D, err_word
+
+
+def last_launch_count() -> int:
+    return int(lib().flce_last_launch_count())
+
+
+def flce_profile_enable(on: bool) -> None:
+    _check(lib().flce_profile_enable(int(bool(on))), "flce_profile_enable")
+
+
+def flce_profile_reset() -> None:
+    lib().flce_profile_reset()
+
+
+def flce_profile_read() -> dict:
+    """{kind: (total_ms, launches)} accumulated since the last reset."""
+    out = {}
+    for k, name in enumerate(PROFILE_KINDS):
+        ms, n = ctypes.c_double(0.0), ctypes.c_int(0)
+        _check(lib().flce_profile_read(k, ctypes.byref(ms), ctypes.byref(n)), "flce_profile_read")
+        out[name] = (ms.value, n.value)
+    return out
+
+
+class _LinearCrossEntropy(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, X, W, labels, ignore_index, smoothing, reduction):
+        loss, lse, nv, err = flce_forward(X, W, labels, ignore_index, smoothing, reduction)
+        ctx.save_for_backward(X, W, labels, lse, nv, err)
+        ctx.cfg = (ignore_index, smoothing, reduction)
+        return loss[0]
+
+    @staticmethod
+    def backward(ctx, g):
+        X, W, labels, lse, nv, err = ctx.saved_tensors
+        ii, eps, red = ctx.cfg
+        g1 = g.reshape(1).to(torch.float32).contiguous()
+        dX, dW, _ = flce_backward(X, W, labels, lse, nv, ii, eps, red, grad_loss=g1, err_word=err)
+        return dX, dW.to(W.dtype), None, None, None, None
+
+
+def linear_cross_entropy(h, W, labels, ignore_index: int = -100, smoothing: float = 0.0,
+                         reduction: str = "mean"):
+    """Autograd entry with the pages' call shape: linear_cross_entropy(h, W, labels,
+    ignore_index=-100).  h may be [..., H]; labels [...] of the same leading shape."""
+    H = h.shape[-1]
+    return _LinearCrossEntropy.apply(h.reshape(-1, H).contiguous(), W.contiguous(),
+                                     labels.reshape(-1).contiguous(), ignore_index, smoothing,
+                                     reduction)

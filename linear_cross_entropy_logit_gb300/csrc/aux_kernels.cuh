@@ -1,0 +1,138 @@
+// Small kernels around the GEMMs: merge of the per-group log-sum-exp
+// partials, the deterministic loss reduction, the gradient scale, the dX
+// down-conversion and the fp32 -> bf16 input cast.
+#pragma once
+#include <cstdint>
+#include <cuda_bf16.h>
+#include "ptx.cuh"
+
+namespace flce {
+
+constexpr int MERGE_THREADS = 256;
+constexpr float LN2 = 0.6931471805599453f;
+
+// One thread per token row.  Merges the vocabulary-group partials
+// (max*log2e, rescaled exp-sum, target logit, logit sum) into
+//   lse_i = m_i + log d_i       ("Chunked and Fused Cross-Entropy ...",
+//                                 "Mathematical Mechanics ...", step 2)
+//   l_i   = valid_i * (lse_i - (1-eps) z_{i,y_i} - (eps/V) sum_j z_ij)
+// and reduces l_i and valid_i over the block in a fixed tree order.
+// A label outside [0, V) that is not ignore_index sets FLCE_ERR_LABEL and
+// the row counts as ignored.
+__global__ void __launch_bounds__(MERGE_THREADS)
+    lse_merge_kernel(const float4* __restrict__ partials, int n_groups, int m_pad, int N, int V,
+                     const int64_t* __restrict__ labels, long long ignore_index, float smoothing,
+                     float* __restrict__ lse_out, double* __restrict__ block_loss,
+                     int* __restrict__ block_valid, int* err_word) {
+  __shared__ double s_loss[MERGE_THREADS];
+  __shared__ int s_valid[MERGE_THREADS];
+  const int row = blockIdx.x * MERGE_THREADS + threadIdx.x;
+  double loss = 0.0;
+  int valid = 0;
+  if (row < N) {
+    float M = -INFINITY;
+    for (int g = 0; g < n_groups; ++g) M = fmaxf(M, partials[(size_t)g * m_pad + row].x);
+    float S = 0.f, zy = 0.f, zs = 0.f;
+    for (int g = 0; g < n_groups; ++g) {
+      const float4 q = partials[(size_t)g * m_pad + row];
+      S += q.y * ex2_approx(q.x - M);
+      zy += q.z;
+      zs += q.w;
+    }
+    const float lse = (M + log2f(S)) * LN2;
+    lse_out[row] = lse;
+    const long long y = labels[row];
+    if (y != ignore_index) {
+      if (y < 0 || y >= V) {
+        record_error(err_word, kErrLabel);
+      } else {
+        valid = 1;
+        double l = (double)lse - (1.0 - (double)smoothing) * (double)zy;
+        if (smoothing != 0.f) l -= (double)smoothing / (double)V * (double)zs;
+        loss = l;
+      }
+    }
+  }
+  s_loss[threadIdx.x] = loss;
+  s_valid[threadIdx.x] = valid;
+  __syncthreads();
+  for (int w = MERGE_THREADS / 2; w > 0; w >>= 1) {
+    if (threadIdx.x < w) {
+      s_loss[threadIdx.x] += s_loss[threadIdx.x + w];
+      s_valid[threadIdx.x] += s_valid[threadIdx.x + w];
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    block_loss[blockIdx.x] = s_loss[0];
+    block_valid[blockIdx.x] = s_valid[0];
+  }
+}
+
+// Single block: fixed-order sum of the block partials, then the mean over
+// valid tokens (0 when none are valid: the chunked reference divides by
+// max(valid_token_count, 1)) or the plain sum.
+__global__ void __launch_bounds__(MERGE_THREADS)
+    loss_finalize_kernel(const double* __restrict__ block_loss, const int* __restrict__ block_valid,
+                         int nblocks, int reduction_sum, float* loss_out, int* valid_out) {
+  __shared__ double s_loss[MERGE_THREADS];
+  __shared__ long long s_valid[MERGE_THREADS];
+  double l = 0.0;
+  long long v = 0;
+  for (int b = threadIdx.x; b < nblocks; b += MERGE_THREADS) {
+    l += block_loss[b];
+    v += block_valid[b];
+  }
+  s_loss[threadIdx.x] = l;
+  s_valid[threadIdx.x] = v;
+  __syncthreads();
+  for (int w = MERGE_THREADS / 2; w > 0; w >>= 1) {
+    if (threadIdx.x < w) {
+      s_loss[threadIdx.x] += s_loss[threadIdx.x + w];
+      s_valid[threadIdx.x] += s_valid[threadIdx.x + w];
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const double total = s_loss[0];
+    const long long nv = s_valid[0];
+    double out = total;
+    if (!reduction_sum) out = nv > 0 ? total / (double)nv : 0.0;
+    *loss_out = (float)out;
+    *valid_out = (int)nv;
+  }
+}
+
+// c = grad / N_valid (mean; 0 when N_valid = 0) or grad (sum); grad defaults to 1.
+__global__ void grad_scale_kernel(const int* valid_count, const float* grad_loss,
+                                  int reduction_sum, float* scale_out) {
+  const float g = grad_loss ? *grad_loss : 1.f;
+  float c = g;
+  if (!reduction_sum) {
+    const int nv = *valid_count;
+    c = nv > 0 ? (float)((double)g / (double)nv) : 0.f;
+  }
+  *scale_out = c;
+}
+
+// dX = bf16(dX_acc), round to nearest even; n4 = number of float4 groups.
+__global__ void dx_finalize_bf16_kernel(const float4* __restrict__ acc, uint2* __restrict__ out,
+                                        size_t n4) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const float4 v = acc[i];
+    out[i] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+  }
+}
+
+// fp32 -> bf16 (round to nearest even), n4 = number of float4 groups.
+__global__ void cast_f32_bf16_kernel(const float4* __restrict__ in, uint2* __restrict__ out,
+                                     size_t n4) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const float4 v = in[i];
+    out[i] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+  }
+}
+
+}  // namespace flce

@@ -1,0 +1,684 @@
+// C-ABI of the fused linear cross-entropy library: argument validation,
+// workspace planning, TMA tensor-map encoding and the stream-ordered launch
+// sequence of the forward and backward passes.
+//
+// Forward (one call):  gemm<kLse>  ->  lse_merge  ->  loss_finalize
+// Backward (one call): grad_scale, then for each vocabulary chunk
+//                      [v0, v0 + Cv):  gemm<kDz> (recompute Z, write dZ chunk)
+//                                      gemm<kStore> dW[v0:v0+Cv] = dZ^T X
+//                                      gemm<kStore> dX_acc += dZ W[v0:v0+Cv]
+//                      then dx_finalize (bf16 inputs).
+// Running the vocabulary chunks outermost lets the dW GEMM contract over all
+// N tokens at once, so every dW row is written exactly once per call (no
+// read-modify-write of the V x H fp32 gradient), while the N x Cv bf16
+// gradient chunk stays the only logit-shaped buffer -- the bounded
+// "scratchpad" of "Chunked and Fused Cross-Entropy ...", step 1, with the
+// roles of rows and vocabulary swapped.
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "flce.h"
+#include "aux_kernels.cuh"
+#include "gemm_core.cuh"
+#include "ptx.cuh"
+
+using namespace flce;
+
+namespace {
+
+constexpr int kStages = 4;
+constexpr int64_t kPartialsBudget = 32ll << 20;   // bytes of forward partials
+constexpr int64_t kDzBudget = 256ll << 20;        // bytes of the dZ chunk (default)
+constexpr unsigned long long kTimeoutNs = 2000000000ull;
+constexpr size_t kAlign = 256;
+
+thread_local std::string g_last_cuda_error;
+thread_local int g_launches = 0;
+std::atomic<int64_t> g_vocab_chunk{0};
+
+// Optional per-kernel timing: CUDA events recorded on the caller's stream
+// around every GEMM launch (kinds: forward logits+LSE, dZ recompute, dW, dX).
+constexpr int kProfKinds = 4;
+struct ProfRec {
+  int kind;
+  cudaEvent_t start, stop;
+};
+thread_local bool g_prof_on = false;
+thread_local std::vector<ProfRec> g_prof_pending;
+thread_local std::vector<cudaEvent_t> g_prof_pool;
+thread_local double g_prof_ms[kProfKinds] = {0, 0, 0, 0};
+thread_local int g_prof_n[kProfKinds] = {0, 0, 0, 0};
+
+cudaEvent_t prof_event() {
+  if (!g_prof_pool.empty()) {
+    cudaEvent_t e = g_prof_pool.back();
+    g_prof_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+flce_status cuda_fail(cudaError_t e, const char* what) {
+  char buf[256];
+  snprintf(buf, sizeof buf, "%s: %s", what, cudaGetErrorString(e));
+  g_last_cuda_error = buf;
+  return FLCE_ERR_CUDA;
+}
+
+#define FLCE_CUDA(call)                                  \
+  do {                                                   \
+    cudaError_t e_ = (call);                             \
+    if (e_ != cudaSuccess) return cuda_fail(e_, #call);  \
+  } while (0)
+
+// ---------------------------------------------------------------------------
+// Workspace plan: depends only on the shape, dtype, mode and chunk setting.
+// ---------------------------------------------------------------------------
+struct Plan {
+  int64_t N, H, V;
+  int m_blocks, m_pad, v_tiles, group_len, n_groups, merge_blocks;
+  int64_t chunk;
+  int n_chunks;
+  size_t off_scalars, off_partials, off_block_loss, off_block_valid, off_dz, off_dxacc,
+      off_xcast, off_wcast, total;
+};
+
+bool shape_ok(int64_t N, int64_t H, int64_t V) {
+  if (N < 0 || H <= 0 || V <= 0) return false;
+  if (H % 8 != 0) return false;
+  // TMA coordinates and the kernels' tile indices are 32-bit.
+  if (N > (int64_t)INT32_MAX - 1024 || V > (int64_t)INT32_MAX - 1024 || H > (int64_t)INT32_MAX)
+    return false;
+  return true;
+}
+
+int64_t auto_chunk(int64_t N, int64_t V) {
+  const int64_t half = std::max<int64_t>(256, (V / 2) / 256 * 256);
+  int64_t set = g_vocab_chunk.load();
+  int64_t c;
+  if (set > 0) {
+    c = ceil_div(set, 256) * 256;
+  } else {
+    c = (kDzBudget / (std::max<int64_t>(N, 1) * 2)) / 256 * 256;
+  }
+  return std::min(std::max<int64_t>(c, 256), half);
+}
+
+bool make_plan(int64_t N, int64_t H, int64_t V, flce_dtype dtype, int mode, Plan* pl) {
+  if (!shape_ok(N, H, V)) return false;
+  if (dtype != FLCE_BF16 && dtype != FLCE_FP32) return false;
+  if (mode < FLCE_MODE_FWD || mode > FLCE_MODE_FWD_BWD) return false;
+  Plan& p = *pl;
+  p.N = N;
+  p.H = H;
+  p.V = V;
+  p.m_blocks = (int)ceil_div(std::max<int64_t>(N, 1), BM);
+  p.m_pad = p.m_blocks * BM;
+  p.v_tiles = (int)ceil_div(V, BN);
+  int L = 1;
+  while ((int64_t)ceil_div(p.v_tiles, L) * p.m_pad * 16 > kPartialsBudget && L < p.v_tiles) L *= 2;
+  p.group_len = L;
+  p.n_groups = (int)ceil_div(p.v_tiles, L);
+  p.merge_blocks = (int)ceil_div(std::max<int64_t>(N, 1), MERGE_THREADS);
+  p.chunk = auto_chunk(N, V);
+  p.n_chunks = (int)ceil_div(V, p.chunk);
+  const bool fwd = mode & FLCE_MODE_FWD;
+  const bool bwd = mode & FLCE_MODE_BWD;
+  size_t off = 0;
+  p.off_scalars = off;
+  off += kAlign;
+  p.off_partials = p.off_block_loss = p.off_block_valid = 0;
+  if (fwd) {
+    p.off_partials = off;
+    off = align_up(off + (size_t)p.n_groups * p.m_pad * sizeof(float4), kAlign);
+    p.off_block_loss = off;
+    off = align_up(off + (size_t)p.merge_blocks * sizeof(double), kAlign);
+    p.off_block_valid = off;
+    off = align_up(off + (size_t)p.merge_blocks * sizeof(int), kAlign);
+  }
+  p.off_dz = p.off_dxacc = 0;
+  if (bwd) {
+    p.off_dz = off;
+    off = align_up(off + (size_t)std::max<int64_t>(N, 1) * p.chunk * 2, kAlign);
+    if (dtype == FLCE_BF16) {
+      p.off_dxacc = off;
+      off = align_up(off + (size_t)N * H * 4, kAlign);
+    }
+  }
+  p.off_xcast = p.off_wcast = 0;
+  if (dtype == FLCE_FP32) {
+    p.off_xcast = off;
+    off = align_up(off + (size_t)N * H * 2, kAlign);
+    p.off_wcast = off;
+    off = align_up(off + (size_t)V * H * 2, kAlign);
+  }
+  p.total = off;
+  return true;
+}
+
+// ---------------------------------------------------------------------------
+// Device properties and kernel attributes (cached per device).
+// ---------------------------------------------------------------------------
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mutex;
+int g_num_sms[kMaxDevices] = {0};
+bool g_dev_ok[kMaxDevices] = {false};
+
+flce_status device_check(int* dev_out, int* sms_out) {
+  int dev = 0;
+  FLCE_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kMaxDevices) return FLCE_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_dev_mutex);
+  if (!g_num_sms[dev]) {
+    int major = 0, minor = 0, sms = 0;
+    FLCE_CUDA(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev));
+    FLCE_CUDA(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev));
+    FLCE_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    g_dev_ok[dev] = (major == 10 && minor == 3);
+    g_num_sms[dev] = sms;
+  }
+  if (!g_dev_ok[dev]) return FLCE_ERR_UNSUPPORTED;
+  *dev_out = dev;
+  *sms_out = g_num_sms[dev];
+  return FLCE_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D tiled tensor map, 128-byte swizzle.  inner/outer in elements.
+flce_status make_map(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void* base,
+                     uint64_t inner, uint64_t outer, uint64_t pitch_bytes, uint32_t box_inner,
+                     uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (!fn) {
+    g_last_cuda_error = "cuTensorMapEncodeTiled entry point unavailable";
+    return FLCE_ERR_CUDA;
+  }
+  (void)elem_bytes;
+  cuuint64_t dims[2] = {inner, std::max<uint64_t>(outer, 1)};
+  cuuint64_t strides[1] = {pitch_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char buf[200];
+    snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled failed (%d): inner=%llu outer=%llu pitch=%llu",
+             (int)r, (unsigned long long)inner, (unsigned long long)outer,
+             (unsigned long long)pitch_bytes);
+    g_last_cuda_error = buf;
+    return FLCE_ERR_CUDA;
+  }
+  return FLCE_OK;
+}
+
+// bf16 operand maps
+flce_status map_kmajor(CUtensorMap* m, const void* base, uint64_t k, uint64_t rows,
+                       uint64_t pitch_elems, uint32_t box_rows) {
+  return make_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, k, rows, pitch_elems * 2, BK,
+                  box_rows);
+}
+flce_status map_mnmajor(CUtensorMap* m, const void* base, uint64_t mn, uint64_t k,
+                        uint64_t pitch_elems) {
+  return make_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, mn, k, pitch_elems * 2, 64, BK);
+}
+// dZ chunk store map: 64 bf16 columns x 32 rows
+flce_status map_dz_store(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
+                         uint64_t pitch_elems) {
+  return make_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, cols, rows, pitch_elems * 2, 64,
+                  32);
+}
+// fp32 output map: 32 columns x 32 rows
+flce_status map_f32_out(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
+                        uint64_t pitch_elems) {
+  return make_map(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, cols, rows, pitch_elems * 4, 32,
+                  32);
+}
+
+template <Epi EPI, bool A_MN, bool B_MN>
+flce_status launch_gemm(int dev, int num_sms, const CUtensorMap& a, const CUtensorMap& b,
+                        const CUtensorMap& out, const GemmParams& p, cudaStream_t st,
+                        int prof_kind = -1) {
+  auto kern = gemm_kernel<EPI, A_MN, B_MN, kStages>;
+  constexpr int smem = gemm_smem_bytes<EPI, kStages>();
+  static std::once_flag flags[kMaxDevices];
+  cudaError_t attr_err = cudaSuccess;
+  std::call_once(flags[dev], [&] {
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  });
+  if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute");
+  if (p.num_units <= 0) return FLCE_OK;
+  const int grid = std::min(p.num_units, num_sms);
+  ProfRec rec{prof_kind, nullptr, nullptr};
+  if (g_prof_on && prof_kind >= 0) {
+    rec.start = prof_event();
+    rec.stop = prof_event();
+    if (rec.start && rec.stop) FLCE_CUDA(cudaEventRecord(rec.start, st));
+  }
+  kern<<<grid, NUM_THREADS, smem, st>>>(a, b, out, p);
+  ++g_launches;
+  FLCE_CUDA(cudaGetLastError());
+  if (rec.start && rec.stop) {
+    FLCE_CUDA(cudaEventRecord(rec.stop, st));
+    g_prof_pending.push_back(rec);
+  }
+  return FLCE_OK;
+}
+
+#define FLCE_TRY(expr)                   \
+  do {                                   \
+    flce_status s_ = (expr);             \
+    if (s_ != FLCE_OK) return s_;        \
+  } while (0)
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct Common {
+  const void* X;
+  const void* W;
+  const int64_t* labels;
+  int64_t N, H, V, ignore_index;
+  float smoothing;
+  flce_dtype dtype;
+  flce_reduction reduction;
+  void* ws;
+  size_t ws_bytes;
+  int32_t* err_word;
+  cudaStream_t st;
+};
+
+flce_status validate_common(const Common& c, int mode, Plan* pl) {
+  if (!shape_ok(c.N, c.H, c.V)) return FLCE_ERR_ARG;
+  if (c.dtype != FLCE_BF16 && c.dtype != FLCE_FP32) return FLCE_ERR_ARG;
+  if (c.reduction != FLCE_MEAN && c.reduction != FLCE_SUM) return FLCE_ERR_ARG;
+  if (!(c.smoothing >= 0.f && c.smoothing < 1.f)) return FLCE_ERR_ARG;
+  if (!c.err_word) return FLCE_ERR_ARG;
+  if (c.N > 0) {
+    if (!c.X || !c.labels) return FLCE_ERR_ARG;
+    if (!aligned(c.X, 16) || !aligned(c.labels, 8)) return FLCE_ERR_ARG;
+  }
+  if (!c.W || !aligned(c.W, 16)) return FLCE_ERR_ARG;
+  if (!aligned(c.err_word, 4)) return FLCE_ERR_ARG;
+  if (!make_plan(c.N, c.H, c.V, c.dtype, mode, pl)) return FLCE_ERR_ARG;
+  if (!c.ws || !aligned(c.ws, kAlign)) return FLCE_ERR_WORKSPACE;
+  if (c.ws_bytes < pl->total) return FLCE_ERR_WORKSPACE;
+  return FLCE_OK;
+}
+
+// fp32 inputs: one rounding to bf16 into the workspace.
+flce_status cast_inputs(const Common& c, const Plan& pl, const void** Xb, const void** Wb) {
+  if (c.dtype == FLCE_BF16) {
+    *Xb = c.X;
+    *Wb = c.W;
+    return FLCE_OK;
+  }
+  uint8_t* ws = static_cast<uint8_t*>(c.ws);
+  void* xo = ws + pl.off_xcast;
+  void* wo = ws + pl.off_wcast;
+  const size_t nx4 = (size_t)c.N * c.H / 4, nw4 = (size_t)c.V * c.H / 4;
+  if (nx4) {
+    cast_f32_bf16_kernel<<<(unsigned)std::min<size_t>(ceil_div(nx4, 256), 4096), 256, 0, c.st>>>(
+        static_cast<const float4*>(c.X), static_cast<uint2*>(xo), nx4);
+    ++g_launches;
+    FLCE_CUDA(cudaGetLastError());
+  }
+  cast_f32_bf16_kernel<<<(unsigned)std::min<size_t>(ceil_div(nw4, 256), 4096), 256, 0, c.st>>>(
+      static_cast<const float4*>(c.W), static_cast<uint2*>(wo), nw4);
+  ++g_launches;
+  FLCE_CUDA(cudaGetLastError());
+  *Xb = xo;
+  *Wb = wo;
+  return FLCE_OK;
+}
+
+flce_status run_forward(const Common& c, const Plan& pl, int dev, int sms, const void* Xb,
+                        const void* Wb, float* loss, float* lse, int32_t* valid_count) {
+  uint8_t* ws = static_cast<uint8_t*>(c.ws);
+  double* block_loss = reinterpret_cast<double*>(ws + pl.off_block_loss);
+  int* block_valid = reinterpret_cast<int*>(ws + pl.off_block_valid);
+  if (c.N > 0) {
+    CUtensorMap tmX, tmW;
+    FLCE_TRY(map_kmajor(&tmX, Xb, c.H, c.N, c.H, BM));
+    FLCE_TRY(map_kmajor(&tmW, Wb, c.H, c.V, c.H, BN));
+    GemmParams p{};
+    p.m_size = (int)c.N;
+    p.n_size = (int)c.V;
+    p.k_size = (int)c.H;
+    p.m_blocks = pl.m_blocks;
+    p.n_blocks = pl.v_tiles;
+    p.group_len = pl.group_len;
+    p.n_groups = pl.n_groups;
+    p.num_units = pl.m_blocks * pl.n_groups;
+    p.m_fastest = 1;
+    p.labels = c.labels;
+    p.ignore_index = c.ignore_index;
+    p.vocab = (int)c.V;
+    p.col_base = 0;
+    p.col_limit = (int)c.V;
+    p.smoothing = c.smoothing;
+    p.partials = reinterpret_cast<float4*>(ws + pl.off_partials);
+    p.m_pad = pl.m_pad;
+    p.err_word = c.err_word;
+    p.timeout_ns = kTimeoutNs;
+    FLCE_TRY((launch_gemm<Epi::kLse, false, false>(dev, sms, tmX, tmW, tmX, p, c.st, 0)));
+    lse_merge_kernel<<<pl.merge_blocks, MERGE_THREADS, 0, c.st>>>(
+        p.partials, pl.n_groups, pl.m_pad, (int)c.N, (int)c.V, c.labels, c.ignore_index,
+        c.smoothing, lse, block_loss, block_valid, c.err_word);
+    ++g_launches;
+    FLCE_CUDA(cudaGetLastError());
+  }
+  loss_finalize_kernel<<<1, MERGE_THREADS, 0, c.st>>>(block_loss, block_valid,
+                                                       c.N > 0 ? pl.merge_blocks : 0,
+                                                       c.reduction == FLCE_SUM, loss, valid_count);
+  ++g_launches;
+  FLCE_CUDA(cudaGetLastError());
+  return FLCE_OK;
+}
+
+flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, const void* Xb,
+                         const void* Wb, const float* lse, const int32_t* valid_count,
+                         const float* grad_loss, void* dX, float* dW, int accumulate) {
+  uint8_t* ws = static_cast<uint8_t*>(c.ws);
+  float* scale = reinterpret_cast<float*>(ws + pl.off_scalars);
+  grad_scale_kernel<<<1, 1, 0, c.st>>>(valid_count, grad_loss, c.reduction == FLCE_SUM, scale);
+  ++g_launches;
+  FLCE_CUDA(cudaGetLastError());
+  if (c.N == 0) {
+    if (!accumulate) FLCE_CUDA(cudaMemsetAsync(dW, 0, (size_t)c.V * c.H * 4, c.st));
+    return FLCE_OK;
+  }
+  const int64_t N = c.N, H = c.H, V = c.V, Cv = pl.chunk;
+  void* dz = ws + pl.off_dz;
+  float* dx_acc = c.dtype == FLCE_BF16 ? reinterpret_cast<float*>(ws + pl.off_dxacc)
+                                       : static_cast<float*>(dX);
+  const auto* Wb16 = static_cast<const uint16_t*>(Wb);
+
+  CUtensorMap tmX_k, tmX_mn, tmDxAcc;
+  FLCE_TRY(map_kmajor(&tmX_k, Xb, H, N, H, BM));
+  FLCE_TRY(map_mnmajor(&tmX_mn, Xb, H, N, H));
+  FLCE_TRY(map_f32_out(&tmDxAcc, dx_acc, H, N, H));
+
+  const int m_blocks_tok = pl.m_blocks;
+  const int h_blocks = (int)ceil_div(H, BN);
+  for (int ci = 0; ci < pl.n_chunks; ++ci) {
+    const int64_t v0 = (int64_t)ci * Cv;
+    const int64_t w = std::min(Cv, V - v0);
+    const void* Wc = Wb16 + v0 * H;
+    CUtensorMap tmWc_k, tmWc_mn, tmDzSt, tmDz_mn, tmDz_k, tmDw;
+    FLCE_TRY(map_kmajor(&tmWc_k, Wc, H, w, H, BN));
+    FLCE_TRY(map_mnmajor(&tmWc_mn, Wc, H, w, H));
+    FLCE_TRY(map_dz_store(&tmDzSt, dz, w, N, Cv));
+    FLCE_TRY(map_mnmajor(&tmDz_mn, dz, w, N, Cv));
+    FLCE_TRY(map_kmajor(&tmDz_k, dz, w, N, Cv, BM));
+    FLCE_TRY(map_f32_out(&tmDw, dW + v0 * H, H, w, H));
+
+    // K3: recompute Z[:, v0:v0+w] and write dZ (bf16) into the chunk scratch.
+    GemmParams p3{};
+    p3.m_size = (int)N;
+    p3.n_size = (int)w;
+    p3.k_size = (int)H;
+    p3.m_blocks = m_blocks_tok;
+    p3.n_blocks = (int)ceil_div(w, BN);
+    p3.group_len = 1;
+    p3.n_groups = p3.n_blocks;
+    p3.num_units = p3.m_blocks * p3.n_groups;
+    p3.m_fastest = 1;
+    p3.labels = c.labels;
+    p3.ignore_index = c.ignore_index;
+    p3.vocab = (int)V;
+    p3.col_base = (int)v0;
+    p3.col_limit = (int)w;
+    p3.smoothing = c.smoothing;
+    p3.lse = lse;
+    p3.scale = scale;
+    p3.err_word = c.err_word;
+    p3.timeout_ns = kTimeoutNs;
+    FLCE_TRY((launch_gemm<Epi::kDz, false, false>(dev, sms, tmX_k, tmWc_k, tmDzSt, p3, c.st, 1)));
+
+    // K4: dW[v0:v0+w, :] = dZ_chunk^T X   (K = N tokens)
+    GemmParams p4{};
+    p4.m_size = (int)w;
+    p4.n_size = (int)H;
+    p4.k_size = (int)N;
+    p4.m_blocks = (int)ceil_div(w, BM);
+    p4.n_blocks = h_blocks;
+    p4.group_len = 1;
+    p4.n_groups = h_blocks;
+    p4.num_units = p4.m_blocks * h_blocks;
+    p4.m_fastest = 0;
+    p4.reduce_add = accumulate ? 1 : 0;
+    p4.err_word = c.err_word;
+    p4.timeout_ns = kTimeoutNs;
+    FLCE_TRY((launch_gemm<Epi::kStore, true, true>(dev, sms, tmDz_mn, tmX_mn, tmDw, p4, c.st, 2)));
+
+    // K5: dX_acc (+)= dZ_chunk W[v0:v0+w, :]   (K = w vocabulary columns)
+    GemmParams p5{};
+    p5.m_size = (int)N;
+    p5.n_size = (int)H;
+    p5.k_size = (int)w;
+    p5.m_blocks = m_blocks_tok;
+    p5.n_blocks = h_blocks;
+    p5.group_len = 1;
+    p5.n_groups = h_blocks;
+    p5.num_units = m_blocks_tok * h_blocks;
+    p5.m_fastest = 0;
+    p5.reduce_add = ci > 0 ? 1 : 0;
+    p5.err_word = c.err_word;
+    p5.timeout_ns = kTimeoutNs;
+    FLCE_TRY((launch_gemm<Epi::kStore, false, true>(dev, sms, tmDz_k, tmWc_mn, tmDxAcc, p5, c.st, 3)));
+  }
+  if (c.dtype == FLCE_BF16) {
+    const size_t n4 = (size_t)N * H / 4;
+    dx_finalize_bf16_kernel<<<(unsigned)std::min<size_t>(ceil_div(n4, 256), 2 * sms), 256, 0,
+                              c.st>>>(reinterpret_cast<const float4*>(dx_acc),
+                                      static_cast<uint2*>(dX), n4);
+    ++g_launches;
+    FLCE_CUDA(cudaGetLastError());
+  }
+  return FLCE_OK;
+}
+
+}  // namespace
+
+// ===========================================================================
+// Exported C ABI
+// ===========================================================================
+extern "C" {
+
+int flce_abi_version(void) { return 100; }
+
+const char* flce_status_string(flce_status s) {
+  switch (s) {
+    case FLCE_OK: return "FLCE_OK";
+    case FLCE_ERR_ARG: return "FLCE_ERR_ARG: invalid argument";
+    case FLCE_ERR_UNSUPPORTED: return "FLCE_ERR_UNSUPPORTED: device or size not supported";
+    case FLCE_ERR_WORKSPACE: return "FLCE_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    case FLCE_ERR_LABEL: return "FLCE_ERR_LABEL: label outside [0, V) and not ignore_index";
+    case FLCE_ERR_TIMEOUT: return "FLCE_ERR_TIMEOUT: a bounded device wait expired";
+    case FLCE_ERR_CUDA: return "FLCE_ERR_CUDA: CUDA call failed";
+  }
+  return "unknown flce_status";
+}
+
+const char* flce_last_cuda_error(void) { return g_last_cuda_error.c_str(); }
+
+int flce_last_launch_count(void) { return g_launches; }
+
+flce_status flce_profile_enable(int on) {
+  g_prof_on = on != 0;
+  return FLCE_OK;
+}
+
+flce_status flce_profile_read(int kind, double* total_ms, int* launches) {
+  if (kind < 0 || kind >= kProfKinds || !total_ms || !launches) return FLCE_ERR_ARG;
+  for (const ProfRec& r : g_prof_pending) {
+    FLCE_CUDA(cudaEventSynchronize(r.stop));
+    float ms = 0.f;
+    FLCE_CUDA(cudaEventElapsedTime(&ms, r.start, r.stop));
+    g_prof_ms[r.kind] += ms;
+    g_prof_n[r.kind] += 1;
+    g_prof_pool.push_back(r.start);
+    g_prof_pool.push_back(r.stop);
+  }
+  g_prof_pending.clear();
+  *total_ms = g_prof_ms[kind];
+  *launches = g_prof_n[kind];
+  return FLCE_OK;
+}
+
+void flce_profile_reset(void) {
+  for (const ProfRec& r : g_prof_pending) {
+    g_prof_pool.push_back(r.start);
+    g_prof_pool.push_back(r.stop);
+  }
+  g_prof_pending.clear();
+  for (int k = 0; k < kProfKinds; ++k) {
+    g_prof_ms[k] = 0.0;
+    g_prof_n[k] = 0;
+  }
+}
+
+flce_status flce_set_vocab_chunk(int64_t cols) {
+  if (cols < 0) return FLCE_ERR_ARG;
+  g_vocab_chunk.store(cols);
+  return FLCE_OK;
+}
+
+int64_t flce_vocab_chunk(int64_t N, int64_t V) {
+  if (N < 0 || V <= 0) return 0;
+  return auto_chunk(N, V);
+}
+
+size_t flce_workspace_size(int64_t N, int64_t H, int64_t V, flce_dtype dtype, int mode) {
+  Plan pl;
+  if (!make_plan(N, H, V, dtype, mode, &pl)) return 0;
+  return pl.total;
+}
+
+flce_status flce_forward(const void* X, const void* W, const int64_t* labels, int64_t N,
+                         int64_t H, int64_t V, int64_t ignore_index, float smoothing,
+                         flce_dtype dtype, flce_reduction reduction, float* loss, float* lse,
+                         int32_t* valid_count, void* workspace, size_t ws_bytes,
+                         int32_t* err_word, void* stream) {
+  g_launches = 0;
+  Common c{X, W, labels, N, H, V, ignore_index, smoothing, dtype, reduction,
+           workspace, ws_bytes, err_word, static_cast<cudaStream_t>(stream)};
+  Plan pl;
+  FLCE_TRY(validate_common(c, FLCE_MODE_FWD, &pl));
+  if (!loss || !valid_count || (N > 0 && !lse)) return FLCE_ERR_ARG;
+  int dev, sms;
+  FLCE_TRY(device_check(&dev, &sms));
+  const void *Xb, *Wb;
+  FLCE_TRY(cast_inputs(c, pl, &Xb, &Wb));
+  return run_forward(c, pl, dev, sms, Xb, Wb, loss, lse, valid_count);
+}
+
+flce_status flce_backward(const void* X, const void* W, const int64_t* labels, int64_t N,
+                          int64_t H, int64_t V, int64_t ignore_index, float smoothing,
+                          flce_dtype dtype, flce_reduction reduction, const float* lse,
+                          const int32_t* valid_count, const float* grad_loss, void* dX,
+                          float* dW, int accumulate_dW, void* workspace, size_t ws_bytes,
+                          int32_t* err_word, void* stream) {
+  g_launches = 0;
+  Common c{X, W, labels, N, H, V, ignore_index, smoothing, dtype, reduction,
+           workspace, ws_bytes, err_word, static_cast<cudaStream_t>(stream)};
+  Plan pl;
+  FLCE_TRY(validate_common(c, FLCE_MODE_BWD, &pl));
+  if (!valid_count || !dW || !aligned(dW, 16)) return FLCE_ERR_ARG;
+  if (N > 0 && (!lse || !dX || !aligned(dX, 16))) return FLCE_ERR_ARG;
+  int dev, sms;
+  FLCE_TRY(device_check(&dev, &sms));
+  const void *Xb, *Wb;
+  FLCE_TRY(cast_inputs(c, pl, &Xb, &Wb));
+  return run_backward(c, pl, dev, sms, Xb, Wb, lse, valid_count, grad_loss, dX, dW,
+                      accumulate_dW);
+}
+
+flce_status flce_fwd_bwd(const void* X, const void* W, const int64_t* labels, int64_t N,
+                         int64_t H, int64_t V, int64_t ignore_index, float smoothing,
+                         flce_dtype dtype, flce_reduction reduction, const float* grad_loss,
+                         float* loss, float* lse, int32_t* valid_count, void* dX, float* dW,
+                         int accumulate_dW, void* workspace, size_t ws_bytes, int32_t* err_word,
+                         void* stream) {
+  g_launches = 0;
+  Common c{X, W, labels, N, H, V, ignore_index, smoothing, dtype, reduction,
+           workspace, ws_bytes, err_word, static_cast<cudaStream_t>(stream)};
+  Plan pl;
+  FLCE_TRY(validate_common(c, FLCE_MODE_FWD_BWD, &pl));
+  if (!loss || !valid_count || !dW || !aligned(dW, 16)) return FLCE_ERR_ARG;
+  if (N > 0 && (!lse || !dX || !aligned(dX, 16))) return FLCE_ERR_ARG;
+  int dev, sms;
+  FLCE_TRY(device_check(&dev, &sms));
+  const void *Xb, *Wb;
+  FLCE_TRY(cast_inputs(c, pl, &Xb, &Wb));
+  FLCE_TRY(run_forward(c, pl, dev, sms, Xb, Wb, loss, lse, valid_count));
+  return run_backward(c, pl, dev, sms, Xb, Wb, lse, valid_count, grad_loss, dX, dW,
+                      accumulate_dW);
+}
+
+flce_status flce_debug_gemm(const void* A, const void* B, float* D, int64_t M, int64_t Nn,
+                            int64_t K, int a_mn, int b_mn, int accumulate, int32_t* err_word,
+                            void* stream) {
+  g_launches = 0;
+  if (!A || !B || !D || !err_word) return FLCE_ERR_ARG;
+  if (M <= 0 || Nn <= 0 || K <= 0 || M > INT32_MAX / 2 || Nn > INT32_MAX / 2 ||
+      K > INT32_MAX / 2)
+    return FLCE_ERR_ARG;
+  if (!aligned(A, 16) || !aligned(B, 16) || !aligned(D, 16)) return FLCE_ERR_ARG;
+  // inner extents of every operand must be 16-byte multiples
+  if ((a_mn ? M : K) % 8 || (b_mn ? Nn : K) % 8 || Nn % 4) return FLCE_ERR_ARG;
+  int dev, sms;
+  FLCE_TRY(device_check(&dev, &sms));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  CUtensorMap ta, tb, td;
+  if (a_mn) FLCE_TRY(map_mnmajor(&ta, A, M, K, M));
+  else FLCE_TRY(map_kmajor(&ta, A, K, M, K, BM));
+  if (b_mn) FLCE_TRY(map_mnmajor(&tb, B, Nn, K, Nn));
+  else FLCE_TRY(map_kmajor(&tb, B, K, Nn, K, BN));
+  FLCE_TRY(map_f32_out(&td, D, Nn, M, Nn));
+  GemmParams p{};
+  p.m_size = (int)M;
+  p.n_size = (int)Nn;
+  p.k_size = (int)K;
+  p.m_blocks = (int)ceil_div(M, BM);
+  p.n_blocks = (int)ceil_div(Nn, BN);
+  p.group_len = 1;
+  p.n_groups = p.n_blocks;
+  p.num_units = p.m_blocks * p.n_blocks;
+  p.m_fastest = 0;
+  p.reduce_add = accumulate ? 1 : 0;
+  p.err_word = err_word;
+  p.timeout_ns = kTimeoutNs;
+  if (!a_mn && !b_mn) return launch_gemm<Epi::kStore, false, false>(dev, sms, ta, tb, td, p, st);
+  if (!a_mn && b_mn) return launch_gemm<Epi::kStore, false, true>(dev, sms, ta, tb, td, p, st);
+  if (a_mn && !b_mn) return launch_gemm<Epi::kStore, true, false>(dev, sms, ta, tb, td, p, st);
+  return launch_gemm<Epi::kStore, true, true>(dev, sms, ta, tb, td, p, st);
+}
+
+}  // extern "C"

@@ -1,0 +1,450 @@
+// Warp-specialised tcgen05 GEMM for sm_103a with the epilogues of the fused
+// linear cross-entropy path.
+//
+// One CTA per SM (persistent), 6 warps:
+//   warp 0      TMA producer (one elected lane): fills a ring of shared-memory
+//               stages with 128x64 A and 256x64 B bf16 tiles (128-byte swizzle)
+//   warp 1      TMEM allocator, then MMA issuer (one elected lane):
+//               tcgen05.mma 128x256x16, fp32 accumulator in TMEM, two
+//               accumulator buffers (2 x 256 columns = all 512 columns) so the
+//               epilogue of tile t overlaps the main loop of tile t+1
+//   warps 2..5  epilogue: warp w reads TMEM lanes 32*(w%4) .. +31, i.e. each
+//               thread owns one row of the 128-row tile
+//
+// D = A * B^T with A: M x K and B: N x K as the MMA sees them.  Either operand
+// may be K-major (K contiguous in memory) or MN-major (M/N contiguous):
+//   forward logits / dZ recompute   Z = X W^T        A = X (K-major), B = W (K-major)
+//   weight gradient                 dW = dZ^T X      A = dZ (MN-major), B = X (MN-major)
+//   input gradient                  dX += dZ W       A = dZ (K-major), B = W (MN-major)
+//
+// Epilogues:
+//   kLse   online log-sum-exp over the tile's vocabulary columns ("Chunked and
+//          Fused Cross-Entropy ...", "Mathematical Mechanics of Chunked Online
+//          Cross-Entropy", step 2; "Fused cross-entropy -- the memory kernel",
+//          "Trick 1 - online softmax"): each thread keeps its row's running max
+//          and rescaled exp-sum across the tiles of a work unit, plus the
+//          target logit and the row sum of logits (label smoothing), and
+//          writes one partial per (vocabulary group, row).  No logit leaves
+//          the SM.
+//   kDz    dZ = c * valid * (exp(z - lse) - (1-eps) 1[j=y] - eps/V)
+//          ("Mathematical Mechanics ...", step 3; "The gradient that makes
+//          fusion trivial"), rounded to bf16 in shared memory and written by
+//          TMA into the bounded N x Cv chunk scratch.
+//   kStore fp32 tile written (or reduce-added) by TMA: the dW and dX GEMMs of
+//          step 4 ("Backward Hidden and Weight Accumulation").
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include "ptx.cuh"
+
+namespace flce {
+
+constexpr int BM = 128;                // tile rows (TMEM lanes)
+constexpr int BN = 256;                // tile columns (TMEM columns per buffer)
+constexpr int BK = 64;                 // bf16 elements per 128-byte row
+constexpr int A_STAGE_BYTES = BM * 128;
+constexpr int B_STAGE_BYTES = BN * 128;
+constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr int MN_BOX_BYTES = 64 * 128;  // one MN-major box: 64 MN elements x 64 k rows
+constexpr int NUM_THREADS = 192;
+constexpr int NUM_EPI_WARPS = 4;
+constexpr int STAGING_BUF_BYTES = 32 * 128;               // 32 rows x 128 bytes
+constexpr int STAGING_BYTES = NUM_EPI_WARPS * 2 * STAGING_BUF_BYTES;
+constexpr int TMEM_COLS = 2 * BN;
+constexpr int BARRIER_BYTES = 256;
+constexpr float LOG2E = 1.4426950408889634f;
+
+enum class Epi : int { kLse = 0, kDz = 1, kStore = 2 };
+
+struct GemmParams {
+  int m_size;      // rows of D
+  int n_size;      // columns of D
+  int k_size;      // contraction length
+  int m_blocks;    // ceil(m_size / BM)
+  int n_blocks;    // ceil(n_size / BN)
+  int group_len;   // consecutive column tiles per work unit
+  int n_groups;    // ceil(n_blocks / group_len)
+  int num_units;   // m_blocks * n_groups
+  int m_fastest;   // 1: consecutive units walk row blocks (share B); 0: walk column groups
+  // kLse / kDz
+  const int64_t* labels;  // per D row (token)
+  long long ignore_index;
+  int vocab;              // V
+  int col_base;           // vocabulary index of D column 0
+  int col_limit;          // D columns >= col_limit do not exist
+  float smoothing;        // eps
+  float4* partials;       // kLse: [n_groups][m_pad] of (max*log2e, sum, z_y, sum_z)
+  int m_pad;              // m_blocks * BM
+  const float* lse;       // kDz: per-row log-sum-exp
+  const float* scale;     // kDz: device scalar c = grad / N_valid
+  // kStore
+  int reduce_add;         // 1: TMA reduce-add onto the output, 0: overwrite
+  // control
+  int* err_word;
+  unsigned long long timeout_ns;
+};
+
+template <Epi EPI, int STAGES>
+constexpr int gemm_smem_bytes() {
+  return STAGES * STAGE_BYTES + (EPI == Epi::kLse ? 0 : STAGING_BYTES) + BARRIER_BYTES + 1024;
+}
+
+__device__ __forceinline__ void unit_coords(const GemmParams& p, int u, int& mb, int& nb0,
+                                            int& nb1, int& g) {
+  if (p.m_fastest) {
+    mb = u % p.m_blocks;
+    g = u / p.m_blocks;
+  } else {
+    g = u % p.n_groups;
+    mb = u / p.n_groups;
+  }
+  nb0 = g * p.group_len;
+  nb1 = min(nb0 + p.group_len, p.n_blocks);
+}
+
+// tcgen05.wait::ld with the loaded registers as operands, so no use of them
+// can be scheduled before the wait.
+__device__ __forceinline__ void tmem_ld_wait_regs(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+                 "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                 "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                 "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+}
+
+// One warp-uniform bounded wait: lane 0 polls, the result is broadcast.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtx& ctx,
+                                          int lane) {
+  int ok = 0;
+  if (lane == 0) ok = mbar_wait(bar, parity, ctx) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  return ok != 0;
+}
+
+// Write one 32-bit-word row of 128 bytes (32 words) into a 128B-swizzled
+// staging buffer: 16-byte chunk c of row r lands at chunk c ^ (r & 7).
+__device__ __forceinline__ void staging_write_row(uint32_t buf, int row, const uint32_t* w) {
+  const uint32_t base = buf + row * 128;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    st_shared_v4(base + ((c ^ (row & 7)) << 4), w[4 * c], w[4 * c + 1], w[4 * c + 2],
+                 w[4 * c + 3]);
+  }
+}
+
+template <Epi EPI, bool A_MN, bool B_MN, int STAGES>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmOut, const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* stages = smem;
+  constexpr int kStaging = (EPI == Epi::kLse) ? 0 : STAGING_BYTES;
+  uint8_t* staging = smem + STAGES * STAGE_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(staging + kStaging);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* mma_done = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], NUM_EPI_WARPS);
+    }
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmB);
+    if (EPI != Epi::kLse) prefetch_tensormap(&tmOut);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const WaitCtx ctx{abort_flag, p.err_word, p.timeout_ns};
+  const int num_kb = (p.k_size + BK - 1) / BK;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+        int mb, nb0, nb1, g;
+        unit_coords(p, u, mb, nb0, nb1, g);
+        for (int nb = nb0; nb < nb1 && ok; ++nb) {
+          for (int kb = 0; kb < num_kb; ++kb) {
+            const int s = it % STAGES;
+            const uint32_t r = it / STAGES;
+            if (!mbar_wait(&empty[s], (r & 1u) ^ 1u, ctx)) {
+              ok = false;
+              break;
+            }
+            uint8_t* a_dst = stages + s * STAGE_BYTES;
+            uint8_t* b_dst = a_dst + A_STAGE_BYTES;
+            mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
+            if constexpr (!A_MN) {
+              tma_load_2d(a_dst, &tmA, &full[s], kb * BK, mb * BM);
+            } else {
+#pragma unroll
+              for (int i = 0; i < BM / 64; ++i)
+                tma_load_2d(a_dst + i * MN_BOX_BYTES, &tmA, &full[s], mb * BM + i * 64, kb * BK);
+            }
+            if constexpr (!B_MN) {
+              tma_load_2d(b_dst, &tmB, &full[s], kb * BK, nb * BN);
+            } else {
+#pragma unroll
+              for (int i = 0; i < BN / 64; ++i)
+                tma_load_2d(b_dst + i * MN_BOX_BYTES, &tmB, &full[s], nb * BN + i * 64, kb * BK);
+            }
+            ++it;
+          }
+        }
+      }
+      if (!ok) {
+        // Drain: the loads of the last (up to) STAGES issued iterations may
+        // still be landing in shared memory.
+        const uint32_t first = it > (uint32_t)STAGES ? it - STAGES : 0u;
+        for (uint32_t j = first; j < it; ++j)
+          mbar_wait_drain(&full[j % STAGES], (j / STAGES) & 1u, p.timeout_ns);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = make_idesc(false, A_MN, B_MN, BM, BN);
+      uint32_t it = 0, tile = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+        int mb, nb0, nb1, g;
+        unit_coords(p, u, mb, nb0, nb1, g);
+        for (int nb = nb0; nb < nb1 && ok; ++nb) {
+          const uint32_t acc = tile & 1u;
+          const uint32_t ra = tile >> 1;
+          if (!mbar_wait(&tempty[acc], (ra & 1u) ^ 1u, ctx)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + acc * BN;
+          for (int kb = 0; kb < num_kb; ++kb) {
+            const int s = it % STAGES;
+            const uint32_t r = it / STAGES;
+            if (!mbar_wait(&full[s], r & 1u, ctx)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_addr = smem_u32(stages + s * STAGE_BYTES);
+            const uint32_t b_addr = a_addr + A_STAGE_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              const uint64_t ad = A_MN ? smem_desc_sw128(a_addr + kk * 2048, MN_BOX_BYTES, 1024)
+                                       : smem_desc_sw128(a_addr + kk * 32, 16, 1024);
+              const uint64_t bd = B_MN ? smem_desc_sw128(b_addr + kk * 2048, MN_BOX_BYTES, 1024)
+                                       : smem_desc_sw128(b_addr + kk * 32, 16, 1024);
+              mma_issue<false>(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            }
+            mma_commit(&empty[s]);
+            ++it;
+          }
+          if (!ok) break;
+          mma_commit(&tfull[acc]);
+          ++tile;
+        }
+      }
+      // Every MMA this thread issued must finish before TMEM is released.
+      mma_commit(mma_done);
+      mbar_wait_drain(mma_done, 0, p.timeout_ns);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;              // TMEM lane quadrant of this warp
+    const int row_in_tile = q * 32 + lane;
+    const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    const uint32_t stag0 = smem_u32(staging) + (warp - 2) * 2 * STAGING_BUF_BYTES;
+    uint32_t tile = 0;
+    bool ok = true;
+    float c_scale = 0.f;
+    if constexpr (EPI == Epi::kDz) c_scale = *p.scale;
+
+    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+      int mb, nb0, nb1, g;
+      unit_coords(p, u, mb, nb0, nb1, g);
+      const int row = mb * BM + row_in_tile;
+      const bool row_ok = row < p.m_size;
+
+      // Per-row state for kLse (natural-log max is m2 / log2(e)).
+      float m2 = -INFINITY, ssum = 0.f, zy = 0.f, zsum = 0.f;
+      long long label = row_ok ? (long long)p.labels[row] : (long long)p.ignore_index;
+      const bool valid = row_ok && label != p.ignore_index;
+      const long long lab_rel = label - p.col_base;
+
+      float dz_coef = 0.f, dz_neg_lse2 = 0.f, dz_eps = 0.f, dz_tgt = 0.f;
+      if constexpr (EPI == Epi::kDz) {
+        const float lse_r = row_ok ? p.lse[row] : 0.f;
+        dz_coef = valid ? c_scale : 0.f;
+        dz_neg_lse2 = -lse_r * LOG2E;
+        dz_eps = dz_coef * p.smoothing / (float)p.vocab;
+        dz_tgt = dz_coef * (1.f - p.smoothing);
+      }
+
+      for (int nb = nb0; nb < nb1; ++nb) {
+        const uint32_t acc = tile & 1u;
+        const uint32_t ra = tile >> 1;
+        if (!warp_wait(&tfull[acc], ra & 1u, ctx, lane)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = lane_base + acc * BN;
+
+        if constexpr (EPI == Epi::kLse) {
+#pragma unroll 1
+          for (int ch = 0; ch < BN / 32; ++ch) {
+            const int c0 = nb * BN + ch * 32;
+            const int nvalid = p.col_limit - c0;  // warp-uniform
+            if (nvalid <= 0) break;
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(taddr + ch * 32, r);
+            tmem_ld_wait_regs(r);
+            float t[32];
+            float cmax = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float z = __uint_as_float(r[j]);
+              t[j] = (j < nvalid) ? z * LOG2E : -INFINITY;
+              cmax = fmaxf(cmax, t[j]);
+            }
+            if (cmax > m2) {
+              ssum *= ex2_approx(m2 - cmax);
+              m2 = cmax;
+            }
+            float part = 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) part += ex2_approx(t[j] - m2);
+            ssum += part;
+            if (p.smoothing != 0.f) {
+              float zs = 0.f;
+#pragma unroll
+              for (int j = 0; j < 32; ++j) zs += (j < nvalid) ? __uint_as_float(r[j]) : 0.f;
+              zsum += zs;
+            }
+            const long long off = lab_rel - c0;
+            if (off >= 0 && off < 32 && off < nvalid) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (j == (int)off) zy = __uint_as_float(r[j]);
+            }
+          }
+        } else if constexpr (EPI == Epi::kDz) {
+#pragma unroll 1
+          for (int sl = 0; sl < BN / 64; ++sl) {
+            const int c0 = nb * BN + sl * 64;
+            if (c0 >= p.col_limit) break;  // warp-uniform; the store would be clipped anyway
+            uint32_t r0[32], r1[32];
+            tmem_ld_32x32b_x32(taddr + sl * 64, r0);
+            tmem_ld_32x32b_x32(taddr + sl * 64 + 32, r1);
+            tmem_ld_wait_regs(r0);
+            tmem_ld_wait_regs(r1);
+            uint32_t w[32];
+            const long long off = lab_rel - c0;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float za = __uint_as_float(r0[j]);
+              const float zb = __uint_as_float(r1[j]);
+              float da = fmaf(dz_coef, ex2_approx(fmaf(za, LOG2E, dz_neg_lse2)), -dz_eps);
+              float db = fmaf(dz_coef, ex2_approx(fmaf(zb, LOG2E, dz_neg_lse2)), -dz_eps);
+              if (off == j) da -= dz_tgt;
+              if (off == j + 32) db -= dz_tgt;
+              r0[j] = __float_as_uint(da);
+              r1[j] = __float_as_uint(db);
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              w[j] = pack_bf16x2(__uint_as_float(r0[2 * j]), __uint_as_float(r0[2 * j + 1]));
+              w[16 + j] = pack_bf16x2(__uint_as_float(r1[2 * j]), __uint_as_float(r1[2 * j + 1]));
+            }
+            const uint32_t buf = stag0 + (sl & 1) * STAGING_BUF_BYTES;
+            if (lane == 0) bulk_wait_group_read<1>();
+            __syncwarp();
+            staging_write_row(buf, lane, w);
+            fence_proxy_async_shared();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmOut, staging + (buf - smem_u32(staging)), c0, mb * BM + q * 32);
+              bulk_commit_group();
+            }
+          }
+        } else {  // kStore
+#pragma unroll 1
+          for (int sl = 0; sl < BN / 32; ++sl) {
+            const int c0 = nb * BN + sl * 32;
+            if (c0 >= p.n_size) break;  // warp-uniform
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(taddr + sl * 32, r);
+            tmem_ld_wait_regs(r);
+            const uint32_t buf = stag0 + (sl & 1) * STAGING_BUF_BYTES;
+            if (lane == 0) bulk_wait_group_read<1>();
+            __syncwarp();
+            staging_write_row(buf, lane, r);
+            fence_proxy_async_shared();
+            __syncwarp();
+            if (lane == 0) {
+              const void* src = staging + (buf - smem_u32(staging));
+              if (p.reduce_add)
+                tma_reduce_add_2d(&tmOut, src, c0, mb * BM + q * 32);
+              else
+                tma_store_2d(&tmOut, src, c0, mb * BM + q * 32);
+              bulk_commit_group();
+            }
+          }
+        }
+
+        // Release the accumulator buffer to the MMA warp.
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+        ++tile;
+      }
+
+      if constexpr (EPI == Epi::kLse) {
+        if (ok) p.partials[(size_t)g * p.m_pad + row] = make_float4(m2, ssum, zy, zsum);
+      }
+    }
+    if constexpr (EPI != Epi::kLse) {
+      if (lane == 0) bulk_wait_group<0>();
+      __syncwarp();
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+}  // namespace flce

@@ -1,0 +1,119 @@
+"""Host-side checks of the C-ABI library: no GPU needed.
+
+The library must load, export every function include/flce.h declares, and plan
+workspaces that never hold an N x V logit-shaped buffer.
+"""
+import ctypes
+import json
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "flce.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from linear_cross_entropy_logit_gb300 import build, binding
+    build.build()
+    return binding.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b(flce_[a-z_0-9]+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_header_exports_all(L):
+    names = declared_functions()
+    assert "flce_forward" in names and "flce_backward" in names and "flce_fwd_bwd" in names
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in flce.h but not exported"
+
+
+def test_status_strings_and_version(L):
+    assert L.flce_abi_version() == 100
+    for s in range(7):
+        assert L.flce_status_string(s).decode().startswith("FLCE_")
+
+
+def test_workspace_plan_bounded():
+    from linear_cross_entropy_logit_gb300 import binding as B
+    from linear_cross_entropy_logit_gb300.inputs import CONFIGS
+    B.flce_set_vocab_chunk(0)
+    for spec in CONFIGS.values():
+        if spec.dtype != "bf16":
+            continue
+        N, H, V = spec.N, spec.H, spec.V
+        cv = B.flce_vocab_chunk(N, V)
+        assert cv % 256 == 0 and 256 <= cv <= V // 2
+        nxv = N * V * 2
+        ws = B.flce_workspace_size(N, H, V, B.FLCE_BF16, B.MODE_FWD_BWD)
+        # the dZ chunk is the only logit-shaped region and is at most half of N x V
+        assert N * cv * 2 <= nxv // 2
+        # whole workspace: dZ chunk + fp32 dX accumulator + forward partials
+        assert ws <= N * cv * 2 + N * H * 4 + (40 << 20)
+        assert ws < nxv
+
+
+def test_workspace_matches_pages_fused_figure():
+    """The dZ chunk at the worked example of "Fused cross-entropy -- the memory
+    kernel" (B*T = 8192, V = 128256, d = 4096) is no larger than one 1024-row
+    chunk of logits the page quotes for the fully fused path (0.26 GB)."""
+    from linear_cross_entropy_logit_gb300 import binding as B
+    figs = json.load(open(os.path.join(ROOT, "tests", "golden", "pages_memory_figures.json")))
+    fused = [f for f in figs["figures"] if f["N"] == 1024 and f["V"] == 128256][0]
+    B.flce_set_vocab_chunk(0)
+    cv = B.flce_vocab_chunk(8192, 128256)
+    assert 8192 * cv * 2 / 1e9 <= fused["printed_gb"] + 0.01
+
+
+def test_workspace_invalid_shapes():
+    from linear_cross_entropy_logit_gb300 import binding as B
+    assert B.flce_workspace_size(10, 12, 100, B.FLCE_BF16, B.MODE_FWD) == 0  # H % 8
+    assert B.flce_workspace_size(-1, 16, 100, B.FLCE_BF16, B.MODE_FWD) == 0
+    assert B.flce_workspace_size(10, 16, 0, B.FLCE_BF16, B.MODE_FWD) == 0
+    assert B.flce_workspace_size(10, 16, 100, 7, B.MODE_FWD) == 0
+    assert B.flce_workspace_size(0, 16, 100, B.FLCE_BF16, B.MODE_FWD_BWD) > 0
+
+
+def test_vocab_chunk_setting():
+    from linear_cross_entropy_logit_gb300 import binding as B
+    try:
+        B.flce_set_vocab_chunk(1000)
+        assert B.flce_vocab_chunk(8192, 128256) == 1024
+        B.flce_set_vocab_chunk(10 ** 9)
+        assert B.flce_vocab_chunk(8192, 128256) == 128256 // 2 // 256 * 256
+    finally:
+        B.flce_set_vocab_chunk(0)
+
+
+def test_argument_errors_without_gpu(L):
+    """Bad arguments are rejected before any CUDA call (so no GPU is needed)."""
+    from linear_cross_entropy_logit_gb300 import binding as B
+    P = ctypes.c_void_p
+    fake = 1 << 20  # aligned non-null addresses; never dereferenced on error
+    # H not a multiple of 8
+    st = L.flce_forward(P(fake), P(fake), P(fake), 4, 12, 16, -100, 0.0, 0, 0, P(fake), P(fake),
+                        P(fake), P(fake), 1 << 20, P(fake), None)
+    assert st == B.FLCE_ERR_ARG
+    # smoothing outside [0, 1)
+    st = L.flce_forward(P(fake), P(fake), P(fake), 4, 16, 16, -100, 1.0, 0, 0, P(fake), P(fake),
+                        P(fake), P(fake), 1 << 20, P(fake), None)
+    assert st == B.FLCE_ERR_ARG
+    # misaligned X
+    st = L.flce_forward(P(fake + 2), P(fake), P(fake), 4, 16, 16, -100, 0.0, 0, 0, P(fake),
+                        P(fake), P(fake), P(fake), 1 << 20, P(fake), None)
+    assert st == B.FLCE_ERR_ARG
+    # workspace too small
+    st = L.flce_forward(P(fake), P(fake), P(fake), 4, 16, 16, -100, 0.0, 0, 0, P(fake), P(fake),
+                        P(fake), P(fake), 16, P(fake), None)
+    assert st == B.FLCE_ERR_WORKSPACE
+    # missing err_word
+    st = L.flce_fwd_bwd(P(fake), P(fake), P(fake), 4, 16, 16, -100, 0.0, 0, 0, None, P(fake),
+                        P(fake), P(fake), P(fake), P(fake), 0, P(fake), 1 << 20, None, None)
+    assert st == B.FLCE_ERR_ARG
