@@ -143,6 +143,29 @@ flce_status flce_profile_enable(int on);
 flce_status flce_profile_read(int kind, double* total_ms, int* launches);
 void flce_profile_reset(void);
 
+/* Forward without any allocation and without a workspace argument.
+ * The pages have no counterpart to this entry point: it exists for callers
+ * that cannot call cudaMalloc or keep a workspace -- code inside a host
+ * application that owns all device memory through its own fixed pool, code
+ * on a path that must not allocate after start-up, and C callers without an
+ * allocator.  Results equal flce_forward's (loss, lse, valid_count, err_word
+ * as there); bf16 X and W only.
+ * Scratch: a fixed device array of FLCE_NOALLOC_SCRATCH_BYTES inside the
+ * library, held on every GPU that runs this entry point until the process
+ * exits.  The first call on a device looks up the array's address (make that
+ * call before any stream capture).  Shapes whose forward partials do not fit
+ * return FLCE_ERR_WORKSPACE (N up to about 1,000,000 tokens fits).  All calls
+ * share the array, so calls whose kernels overlap on the GPU (other streams
+ * or host threads) race: serialise them. */
+#define FLCE_NOALLOC_SCRATCH_BYTES (16u << 20)
+flce_status flce_forward_noalloc(const void* X, const void* W, const int64_t* labels, int64_t N,
+                                 int64_t H, int64_t V, int64_t ignore_index, float smoothing,
+                                 flce_reduction reduction, float* loss, float* lse,
+                                 int32_t* valid_count, int32_t* err_word, void* stream);
+
+/* Text of the last error flce_forward_noalloc met on this thread ("" if none). */
+const char* flce_noalloc_last_error(void);
+
 /* ABI version of this header (major * 100 + minor). */
 int flce_abi_version(void);
 

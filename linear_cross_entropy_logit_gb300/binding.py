@@ -35,7 +35,7 @@ EXPORTED = (
     "flce_workspace_size", "flce_set_vocab_chunk", "flce_vocab_chunk", "flce_forward",
     "flce_backward", "flce_fwd_bwd", "flce_status_string", "flce_last_cuda_error",
     "flce_last_launch_count", "flce_abi_version", "flce_debug_gemm", "flce_profile_enable",
-    "flce_profile_read", "flce_profile_reset",
+    "flce_profile_read", "flce_profile_reset", "flce_forward_noalloc", "flce_noalloc_last_error",
 )
 
 PROFILE_KINDS = ("fwd_logits_lse", "bwd_dz_recompute", "bwd_dw_gemm", "bwd_dx_gemm")
@@ -93,6 +93,10 @@ def lib() -> ctypes.CDLL:
     L.flce_profile_read.restype = I32
     L.flce_profile_reset.argtypes = []
     L.flce_profile_reset.restype = None
+    L.flce_forward_noalloc.argtypes = [P, P, P, I64, I64, I64, I64, F32, I32, P, P, P, P, P]
+    L.flce_forward_noalloc.restype = I32
+    L.flce_noalloc_last_error.argtypes = []
+    L.flce_noalloc_last_error.restype = ctypes.c_char_p
     _lib = L
     return L
 
@@ -243,6 +247,24 @@ def flce_debug_gemm(A, B, M: int, Nn: int, K: int, a_mn: bool, b_mn: bool, D=Non
                                int(accumulate), _ptr(err_word), _stream(stream))
     _check(st, "flce_debug_gemm")
     return D, err_word
+
+
+def flce_forward_noalloc(X, W, labels, ignore_index: int = -100, smoothing: float = 0.0,
+                         reduction: str = "mean", *, loss, lse, valid_count, err_word,
+                         stream=None):
+    """Forward for callers that cannot allocate: every output buffer is the
+    caller's and no workspace is passed (the library uses its own fixed device
+    scratch).  bf16 X and W only.  Returns (loss, lse, valid_count, err_word)."""
+    N, H, V = _check_inputs(X, W, labels)
+    if X.dtype != torch.bfloat16:
+        raise TypeError("flce_forward_noalloc takes bf16 X and W")
+    st = lib().flce_forward_noalloc(_ptr(X), _ptr(W), _ptr(labels), N, H, V, ignore_index,
+                                    smoothing, _red_code(reduction), _ptr(loss), _ptr(lse),
+                                    _ptr(valid_count), _ptr(err_word), _stream(stream))
+    if st != FLCE_OK:
+        raise RuntimeError(f"flce_forward_noalloc: {lib().flce_status_string(st).decode()} "
+                           f"({lib().flce_noalloc_last_error().decode()})")
+    return loss, lse, valid_count, err_word
 
 
 def last_launch_count() -> int:

@@ -19,7 +19,7 @@ constexpr float LN2 = 0.6931471805599453f;
 // and reduces l_i and valid_i over the block in a fixed tree order.
 // A label outside [0, V) that is not ignore_index sets FLCE_ERR_LABEL and
 // the row counts as ignored.
-__global__ void __launch_bounds__(MERGE_THREADS)
+static __global__ void __launch_bounds__(MERGE_THREADS)
     lse_merge_kernel(const float4* __restrict__ partials, int n_groups, int m_pad, int N, int V,
                      const int64_t* __restrict__ labels, long long ignore_index, float smoothing,
                      float* __restrict__ lse_out, double* __restrict__ block_loss,
@@ -72,7 +72,7 @@ __global__ void __launch_bounds__(MERGE_THREADS)
 // Single block: fixed-order sum of the block partials, then the mean over
 // valid tokens (0 when none are valid: the chunked reference divides by
 // max(valid_token_count, 1)) or the plain sum.
-__global__ void __launch_bounds__(MERGE_THREADS)
+static __global__ void __launch_bounds__(MERGE_THREADS)
     loss_finalize_kernel(const double* __restrict__ block_loss, const int* __restrict__ block_valid,
                          int nblocks, int reduction_sum, float* loss_out, int* valid_out) {
   __shared__ double s_loss[MERGE_THREADS];
@@ -104,7 +104,7 @@ __global__ void __launch_bounds__(MERGE_THREADS)
 }
 
 // c = grad / N_valid (mean; 0 when N_valid = 0) or grad (sum); grad defaults to 1.
-__global__ void grad_scale_kernel(const int* valid_count, const float* grad_loss,
+static __global__ void grad_scale_kernel(const int* valid_count, const float* grad_loss,
                                   int reduction_sum, float* scale_out) {
   const float g = grad_loss ? *grad_loss : 1.f;
   float c = g;
@@ -116,7 +116,7 @@ __global__ void grad_scale_kernel(const int* valid_count, const float* grad_loss
 }
 
 // dX = bf16(dX_acc), round to nearest even; n4 = number of float4 groups.
-__global__ void dx_finalize_bf16_kernel(const float4* __restrict__ acc, uint2* __restrict__ out,
+static __global__ void dx_finalize_bf16_kernel(const float4* __restrict__ acc, uint2* __restrict__ out,
                                         size_t n4) {
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4;
        i += (size_t)gridDim.x * blockDim.x) {
@@ -126,7 +126,7 @@ __global__ void dx_finalize_bf16_kernel(const float4* __restrict__ acc, uint2* _
 }
 
 // fp32 -> bf16 (round to nearest even), n4 = number of float4 groups.
-__global__ void cast_f32_bf16_kernel(const float4* __restrict__ in, uint2* __restrict__ out,
+static __global__ void cast_f32_bf16_kernel(const float4* __restrict__ in, uint2* __restrict__ out,
                                      size_t n4) {
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4;
        i += (size_t)gridDim.x * blockDim.x) {
