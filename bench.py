@@ -35,11 +35,14 @@ DEFAULT_WORKLOAD = "llama3_n8192"
 def parse_args():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--shape", default=None,
+                    help="N,H,V override of the workload's shape (same input recipe); "
+                         "for small profiler captures")
     ap.add_argument("--vocab-chunk", type=int, default=0,
                     help="vocabulary columns per backward chunk (0 = automatic)")
     ap.add_argument("--cpu-baseline-rows", type=int, default=1024,
@@ -136,7 +139,7 @@ def run_reference(args, rank: int):
     from linear_cross_entropy_logit_gb300 import inputs as I
     if rank != 0:
         return
-    spec = I.CONFIGS[args.workload]
+    spec = workload_spec(args)
     wl = I.make_workload(spec, seed=args.seed)
     for _ in range(args.warmup):
         oracle_sample(wl, args.reference_rows)
@@ -161,6 +164,18 @@ def run_reference(args, rank: int):
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+def workload_spec(args):
+    import dataclasses
+    from linear_cross_entropy_logit_gb300 import inputs as I
+    spec = I.CONFIGS[args.workload]
+    if args.shape:
+        N, H, V = (int(v) for v in args.shape.split(","))
+        spec = dataclasses.replace(spec, name=f"{spec.name}@{N}x{H}x{V}", N=N, H=H, V=V,
+                                   n_ignore=min(spec.n_ignore, N),
+                                   n_scaled_w_rows=min(spec.n_scaled_w_rows, V))
+    return spec
 
 
 def workload_config(spec, chunk):
@@ -197,7 +212,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    spec = I.CONFIGS[args.workload]
+    spec = workload_spec(args)
     wl = I.make_workload(spec, seed=args.seed + rank)
     N, H, V = spec.N, spec.H, spec.V
     B.flce_set_vocab_chunk(args.vocab_chunk)
@@ -212,7 +227,6 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     yh = torch.from_numpy(wl.labels)
     X, W, y = Xh.to(dev), Wh.to(dev), yh.to(dev)
     dt = B.FLCE_BF16 if spec.dtype == "bf16" else B.FLCE_FP32
-    ws = B.workspace(N, H, V, dt, B.MODE_FWD_BWD, dev)
     loss = torch.empty(1, dtype=torch.float32, device=dev)
     lse = torch.empty(N, dtype=torch.float32, device=dev)
     nv = torch.empty(1, dtype=torch.int32, device=dev)
@@ -220,7 +234,10 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     dW = torch.empty(V, H, dtype=torch.float32, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    base_mem = torch.cuda.memory_allocated(dev)
+    torch.cuda.synchronize(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    base_mem = torch.cuda.memory_allocated(dev)  # inputs and outputs only
+    ws = B.workspace(N, H, V, dt, B.MODE_FWD_BWD, dev)
 
     def step():
         B.flce_fwd_bwd(X, W, y, spec.ignore_index, spec.smoothing, spec.reduction, loss=loss,
@@ -255,6 +272,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     if world > 1:
         dist.barrier()
     clocks = sampler.stop() if sampler else None
+    peak_extra = torch.cuda.max_memory_allocated(dev) - base_mem
     B.flce_profile_enable(False)
     prof = B.flce_profile_read()
     ms = ev0.elapsed_time(ev1)
@@ -351,7 +369,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     extra = {"workspace_bytes": ws.numel(),
              "workspace_vs_nxv_bf16": ws.numel() / (N * V * 2),
              "dz_chunk_bytes": N * chunk * 2,
-             "peak_extra_device_bytes": torch.cuda.max_memory_allocated(dev) - base_mem}
+             "peak_extra_device_bytes": peak_extra,
+             "nxv_bf16_bytes": N * V * 2}
     line = {
         "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,

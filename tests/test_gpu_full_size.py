@@ -1,0 +1,70 @@
+"""Parity at the full workload sizes, in the launch configuration bench.py times.
+
+One flce_fwd_bwd call per workload (default vocabulary chunk).  Against the
+fp64 oracle:
+  * the loss and the lse of every token row (the oracle's full forward);
+  * dX on sampled token rows, ignored rows included (exactly zero there);
+  * dW on sampled vocabulary rows (the most frequent labels, random rows, and
+    for the Gemma-shaped workload some of the x8-scaled rows), each computed
+    by the oracle one by one from its own lse;
+  * the property sum_j dW_j = 0 on the whole GPU dW, relative to sum_j |dW_j|.
+Each case takes from ~20 s (Llama shape) to ~2 min (Gemma shape) of oracle time
+on the host.
+"""
+import numpy as np
+import pytest
+
+from linear_cross_entropy_logit_gb300 import inputs as I
+from oracle import flce_oracle as O
+from tests.gpu_util import GRAD_REL_FRO, LOSS_REL, LSE_ABS, rel_err, rel_fro, to_device
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+WORKLOADS = ["llama3_n8192", "llama3_long_n16384", "qwen25_n16384", "gemma2_n32768"]
+
+
+@pytest.mark.parametrize("name", WORKLOADS)
+def test_full_size_parity(name):
+    import torch
+    from linear_cross_entropy_logit_gb300 import binding as B
+
+    B.flce_set_vocab_chunk(0)
+    spec = I.CONFIGS[name]
+    wl = I.make_workload(spec, seed=0)
+    N, V = spec.N, spec.V
+    ii, eps = spec.ignore_index, spec.smoothing
+    X, W, y = to_device(wl)
+    loss, lse, nv, dX, dW, err = B.flce_fwd_bwd(X, W, y, ii, eps, spec.reduction)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    got_lse = lse.double().cpu().numpy()
+
+    rng = np.random.default_rng(1234)
+    ignored = np.flatnonzero(wl.labels == ii)
+    rows = np.unique(np.concatenate([ignored[:8], rng.choice(N, 56, replace=False)]))
+    labels_valid = wl.labels[wl.labels != ii]
+    counts = np.bincount(labels_valid, minlength=V)
+    vrows = [np.argsort(-counts)[:8], rng.choice(V, 40, replace=False)]
+    if spec.n_scaled_w_rows:
+        scaled = I._rng(0, 5).permutation(V)[:spec.n_scaled_w_rows]
+        vrows.append(scaled[:8])
+    vrows = np.unique(np.concatenate(vrows))
+    got_dx = dX[torch.from_numpy(rows).cuda()].double().cpu().numpy()
+    got_dw = dW[torch.from_numpy(vrows).cuda()].double().cpu().numpy()
+    # sum_j dW_j = 0 on the whole GPU output, relative to sum_j |dW_j|
+    col_sum = dW.double().sum(dim=0).norm().item()
+    row_norm_sum = dW.double().norm(dim=1).sum().item()
+    del X, W, dX, dW
+    torch.cuda.empty_cache()
+
+    f = O.forward(wl.x, wl.w, wl.labels, ii, eps, spec.reduction)
+    assert int(nv.item()) == f.n_valid
+    assert rel_err(loss.item(), f.loss) <= LOSS_REL, (loss.item(), f.loss)
+    assert np.max(np.abs(got_lse - f.lse)) <= LSE_ABS
+    c = O.grad_scale(f.n_valid, spec.reduction)
+    want_dx = O.dx_rows(wl.x, wl.w, wl.labels, rows, c, ii, eps)
+    assert rel_fro(got_dx, want_dx) <= GRAD_REL_FRO
+    assert np.all(got_dx[np.isin(rows, ignored)] == 0.0)
+    want_dw = O.dw_rows(wl.x, wl.w, wl.labels, vrows, f.lse, c, ii, eps)
+    assert rel_fro(got_dw, want_dw) <= GRAD_REL_FRO
+    assert col_sum / row_norm_sum <= 1e-3
