@@ -90,6 +90,13 @@ size_t flce_workspace_size(int64_t N, int64_t H, int64_t V, flce_dtype dtype, in
 flce_status flce_set_vocab_chunk(int64_t cols);
 int64_t flce_vocab_chunk(int64_t N, int64_t V);
 
+/* GEMM tile shape, process-wide.  1 (the default): a cluster of two CTAs on
+ * two SMs computes each 256 x 256 tile with tcgen05.mma.cta_group::2, each CTA
+ * loading its own 128 rows of A and half of B.  0: one CTA per 128 x 256 tile.
+ * Both give the same results up to fp32 summation order. */
+flce_status flce_set_cta_pair(int on);
+int flce_cta_pair(void);
+
 /* Forward ("Mathematical Mechanics of Chunked Online Cross-Entropy", steps
  * 1-2): loss (device float, 1), lse (device float, N, every row including
  * ignored ones), valid_count (device int32, 1: N_valid).  workspace: device,

@@ -34,7 +34,8 @@ using namespace flce;
 
 namespace {
 
-constexpr int kStages = 4;
+constexpr int kStages = 4;       // 1-CTA tiles: 4 x 48 KB stages
+constexpr int kPairStages = 6;   // CTA-pair tiles: 6 x 32 KB stages per CTA
 constexpr int64_t kPartialsBudget = 32ll << 20;   // bytes of forward partials
 constexpr int64_t kDzBudget = 256ll << 20;        // bytes of the dZ chunk (default)
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
@@ -43,6 +44,7 @@ constexpr size_t kAlign = 256;
 thread_local std::string g_last_cuda_error;
 thread_local int g_launches = 0;
 std::atomic<int64_t> g_vocab_chunk{0};
+std::atomic<int> g_cta_pair{1};
 
 // Optional per-kernel timing: CUDA events recorded on the caller's stream
 // around every GEMM launch (kinds: forward logits+LSE, dZ recompute, dW, dX).
@@ -125,8 +127,8 @@ bool make_plan(int64_t N, int64_t H, int64_t V, flce_dtype dtype, int mode, Plan
   p.N = N;
   p.H = H;
   p.V = V;
-  p.m_blocks = (int)ceil_div(std::max<int64_t>(N, 1), BM);
-  p.m_pad = p.m_blocks * BM;
+  p.m_blocks = (int)ceil_div(std::max<int64_t>(N, 1), 2 * BM);
+  p.m_pad = p.m_blocks * 2 * BM;  // covers the row padding of either tile shape
   p.v_tiles = (int)ceil_div(V, BN);
   int L = 1;
   while ((int64_t)ceil_div(p.v_tiles, L) * p.m_pad * 16 > kPartialsBudget && L < p.v_tiles) L *= 2;
@@ -261,12 +263,18 @@ flce_status map_f32_out(CUtensorMap* m, const void* base, uint64_t cols, uint64_
                   32);
 }
 
-template <Epi EPI, bool A_MN, bool B_MN>
+template <Epi EPI, bool A_MN, bool B_MN, bool PAIR>
 flce_status launch_gemm(int dev, int num_sms, const CUtensorMap& a, const CUtensorMap& b,
                         const CUtensorMap& out, const GemmParams& p, cudaStream_t st,
                         int prof_kind = -1) {
-  auto kern = gemm_kernel<EPI, A_MN, B_MN, kStages>;
-  constexpr int smem = gemm_smem_bytes<EPI, kStages>();
+  constexpr int stages = PAIR ? kPairStages : kStages;
+  auto kern = [] {
+    if constexpr (PAIR)
+      return gemm_pair_kernel<EPI, A_MN, B_MN, stages>;
+    else
+      return gemm_kernel<EPI, A_MN, B_MN, stages>;
+  }();
+  constexpr int smem = gemm_smem_bytes<EPI, stages, PAIR>();
   static std::once_flag flags[kMaxDevices];
   cudaError_t attr_err = cudaSuccess;
   std::call_once(flags[dev], [&] {
@@ -274,7 +282,23 @@ flce_status launch_gemm(int dev, int num_sms, const CUtensorMap& a, const CUtens
   });
   if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute");
   if (p.num_units <= 0) return FLCE_OK;
-  const int grid = std::min(p.num_units, num_sms);
+  // One CTA per SM (one cluster per SM pair), persistent over the work units.
+  // A persistent grid must be co-resident, so pairs are capped by how many
+  // 2-CTA clusters of this size fit on the device at once.
+  int grid = std::min(p.num_units, num_sms);
+  if constexpr (PAIR) {
+    static int max_clusters[kMaxDevices] = {0};
+    if (max_clusters[dev] == 0) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
+      cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+      cfg.dynamicSmemBytes = smem;
+      int n = 0;
+      FLCE_CUDA(cudaOccupancyMaxActiveClusters(&n, kern, &cfg));
+      max_clusters[dev] = std::max(1, std::min(n, num_sms / 2));
+    }
+    grid = 2 * std::min(p.num_units, max_clusters[dev]);
+  }
   ProfRec rec{prof_kind, nullptr, nullptr};
   if (g_prof_on && prof_kind >= 0) {
     rec.start = prof_event();
@@ -290,6 +314,19 @@ flce_status launch_gemm(int dev, int num_sms, const CUtensorMap& a, const CUtens
   }
   return FLCE_OK;
 }
+
+// Run-time choice between the 1-CTA (128 x 256) and CTA-pair (256 x 256) kernels.
+template <Epi EPI, bool A_MN, bool B_MN>
+flce_status launch_tile(bool pair, int dev, int num_sms, const CUtensorMap& a,
+                        const CUtensorMap& b, const CUtensorMap& out, const GemmParams& p,
+                        cudaStream_t st, int prof_kind = -1) {
+  return pair ? launch_gemm<EPI, A_MN, B_MN, true>(dev, num_sms, a, b, out, p, st, prof_kind)
+              : launch_gemm<EPI, A_MN, B_MN, false>(dev, num_sms, a, b, out, p, st, prof_kind);
+}
+
+bool use_pair() { return g_cta_pair.load() != 0; }
+int tile_rows(bool pair) { return pair ? 2 * BM : BM; }
+uint32_t b_box_rows(bool pair) { return pair ? BN / 2 : BN; }
 
 #define FLCE_TRY(expr)                   \
   do {                                   \
@@ -363,18 +400,19 @@ flce_status run_forward(const Common& c, const Plan& pl, int dev, int sms, const
   double* block_loss = reinterpret_cast<double*>(ws + pl.off_block_loss);
   int* block_valid = reinterpret_cast<int*>(ws + pl.off_block_valid);
   if (c.N > 0) {
+    const bool pair = use_pair();
     CUtensorMap tmX, tmW;
     FLCE_TRY(map_kmajor(&tmX, Xb, c.H, c.N, c.H, BM));
-    FLCE_TRY(map_kmajor(&tmW, Wb, c.H, c.V, c.H, BN));
+    FLCE_TRY(map_kmajor(&tmW, Wb, c.H, c.V, c.H, b_box_rows(pair)));
     GemmParams p{};
     p.m_size = (int)c.N;
     p.n_size = (int)c.V;
     p.k_size = (int)c.H;
-    p.m_blocks = pl.m_blocks;
+    p.m_blocks = (int)ceil_div(c.N, tile_rows(pair));
     p.n_blocks = pl.v_tiles;
     p.group_len = pl.group_len;
     p.n_groups = pl.n_groups;
-    p.num_units = pl.m_blocks * pl.n_groups;
+    p.num_units = p.m_blocks * pl.n_groups;
     p.m_fastest = 1;
     p.labels = c.labels;
     p.ignore_index = c.ignore_index;
@@ -386,7 +424,7 @@ flce_status run_forward(const Common& c, const Plan& pl, int dev, int sms, const
     p.m_pad = pl.m_pad;
     p.err_word = c.err_word;
     p.timeout_ns = kTimeoutNs;
-    FLCE_TRY((launch_gemm<Epi::kLse, false, false>(dev, sms, tmX, tmW, tmX, p, c.st, 0)));
+    FLCE_TRY((launch_tile<Epi::kLse, false, false>(pair, dev, sms, tmX, tmW, tmX, p, c.st, 0)));
     lse_merge_kernel<<<pl.merge_blocks, MERGE_THREADS, 0, c.st>>>(
         p.partials, pl.n_groups, pl.m_pad, (int)c.N, (int)c.V, c.labels, c.ignore_index,
         c.smoothing, lse, block_loss, block_valid, c.err_word);
@@ -424,14 +462,15 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
   FLCE_TRY(map_mnmajor(&tmX_mn, Xb, H, N, H));
   FLCE_TRY(map_f32_out(&tmDxAcc, dx_acc, H, N, H));
 
-  const int m_blocks_tok = pl.m_blocks;
+  const bool pair = use_pair();
+  const int m_blocks_tok = (int)ceil_div(N, tile_rows(pair));
   const int h_blocks = (int)ceil_div(H, BN);
   for (int ci = 0; ci < pl.n_chunks; ++ci) {
     const int64_t v0 = (int64_t)ci * Cv;
     const int64_t w = std::min(Cv, V - v0);
     const void* Wc = Wb16 + v0 * H;
     CUtensorMap tmWc_k, tmWc_mn, tmDzSt, tmDz_mn, tmDz_k, tmDw;
-    FLCE_TRY(map_kmajor(&tmWc_k, Wc, H, w, H, BN));
+    FLCE_TRY(map_kmajor(&tmWc_k, Wc, H, w, H, b_box_rows(pair)));
     FLCE_TRY(map_mnmajor(&tmWc_mn, Wc, H, w, H));
     FLCE_TRY(map_dz_store(&tmDzSt, dz, w, N, Cv));
     FLCE_TRY(map_mnmajor(&tmDz_mn, dz, w, N, Cv));
@@ -459,14 +498,14 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
     p3.scale = scale;
     p3.err_word = c.err_word;
     p3.timeout_ns = kTimeoutNs;
-    FLCE_TRY((launch_gemm<Epi::kDz, false, false>(dev, sms, tmX_k, tmWc_k, tmDzSt, p3, c.st, 1)));
+    FLCE_TRY((launch_tile<Epi::kDz, false, false>(pair, dev, sms, tmX_k, tmWc_k, tmDzSt, p3, c.st, 1)));
 
     // K4: dW[v0:v0+w, :] = dZ_chunk^T X   (K = N tokens)
     GemmParams p4{};
     p4.m_size = (int)w;
     p4.n_size = (int)H;
     p4.k_size = (int)N;
-    p4.m_blocks = (int)ceil_div(w, BM);
+    p4.m_blocks = (int)ceil_div(w, tile_rows(pair));
     p4.n_blocks = h_blocks;
     p4.group_len = 1;
     p4.n_groups = h_blocks;
@@ -475,7 +514,7 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
     p4.reduce_add = accumulate ? 1 : 0;
     p4.err_word = c.err_word;
     p4.timeout_ns = kTimeoutNs;
-    FLCE_TRY((launch_gemm<Epi::kStore, true, true>(dev, sms, tmDz_mn, tmX_mn, tmDw, p4, c.st, 2)));
+    FLCE_TRY((launch_tile<Epi::kStore, true, true>(pair, dev, sms, tmDz_mn, tmX_mn, tmDw, p4, c.st, 2)));
 
     // K5: dX_acc (+)= dZ_chunk W[v0:v0+w, :]   (K = w vocabulary columns)
     GemmParams p5{};
@@ -491,7 +530,7 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
     p5.reduce_add = ci > 0 ? 1 : 0;
     p5.err_word = c.err_word;
     p5.timeout_ns = kTimeoutNs;
-    FLCE_TRY((launch_gemm<Epi::kStore, false, true>(dev, sms, tmDz_k, tmWc_mn, tmDxAcc, p5, c.st, 3)));
+    FLCE_TRY((launch_tile<Epi::kStore, false, true>(pair, dev, sms, tmDz_k, tmWc_mn, tmDxAcc, p5, c.st, 3)));
   }
   if (c.dtype == FLCE_BF16) {
     const size_t n4 = (size_t)N * H / 4;
@@ -511,7 +550,7 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
 // ===========================================================================
 extern "C" {
 
-int flce_abi_version(void) { return 100; }
+int flce_abi_version(void) { return 101; }
 
 const char* flce_status_string(flce_status s) {
   switch (s) {
@@ -563,6 +602,13 @@ void flce_profile_reset(void) {
     g_prof_n[k] = 0;
   }
 }
+
+flce_status flce_set_cta_pair(int on) {
+  g_cta_pair.store(on != 0 ? 1 : 0);
+  return FLCE_OK;
+}
+
+int flce_cta_pair(void) { return g_cta_pair.load(); }
 
 flce_status flce_set_vocab_chunk(int64_t cols) {
   if (cols < 0) return FLCE_ERR_ARG;
@@ -660,13 +706,14 @@ flce_status flce_debug_gemm(const void* A, const void* B, float* D, int64_t M, i
   if (a_mn) FLCE_TRY(map_mnmajor(&ta, A, M, K, M));
   else FLCE_TRY(map_kmajor(&ta, A, K, M, K, BM));
   if (b_mn) FLCE_TRY(map_mnmajor(&tb, B, Nn, K, Nn));
-  else FLCE_TRY(map_kmajor(&tb, B, K, Nn, K, BN));
+  else FLCE_TRY(map_kmajor(&tb, B, K, Nn, K, b_box_rows(use_pair())));
   FLCE_TRY(map_f32_out(&td, D, Nn, M, Nn));
   GemmParams p{};
   p.m_size = (int)M;
   p.n_size = (int)Nn;
   p.k_size = (int)K;
-  p.m_blocks = (int)ceil_div(M, BM);
+  const bool pair = use_pair();
+  p.m_blocks = (int)ceil_div(M, tile_rows(pair));
   p.n_blocks = (int)ceil_div(Nn, BN);
   p.group_len = 1;
   p.n_groups = p.n_blocks;
@@ -675,10 +722,10 @@ flce_status flce_debug_gemm(const void* A, const void* B, float* D, int64_t M, i
   p.reduce_add = accumulate ? 1 : 0;
   p.err_word = err_word;
   p.timeout_ns = kTimeoutNs;
-  if (!a_mn && !b_mn) return launch_gemm<Epi::kStore, false, false>(dev, sms, ta, tb, td, p, st);
-  if (!a_mn && b_mn) return launch_gemm<Epi::kStore, false, true>(dev, sms, ta, tb, td, p, st);
-  if (a_mn && !b_mn) return launch_gemm<Epi::kStore, true, false>(dev, sms, ta, tb, td, p, st);
-  return launch_gemm<Epi::kStore, true, true>(dev, sms, ta, tb, td, p, st);
+  if (!a_mn && !b_mn) return launch_tile<Epi::kStore, false, false>(pair, dev, sms, ta, tb, td, p, st);
+  if (!a_mn && b_mn) return launch_tile<Epi::kStore, false, true>(pair, dev, sms, ta, tb, td, p, st);
+  if (a_mn && !b_mn) return launch_tile<Epi::kStore, true, false>(pair, dev, sms, ta, tb, td, p, st);
+  return launch_tile<Epi::kStore, true, true>(pair, dev, sms, ta, tb, td, p, st);
 }
 
 }  // extern "C"

@@ -1,15 +1,25 @@
 // Warp-specialised tcgen05 GEMM for sm_103a with the epilogues of the fused
 // linear cross-entropy path.
 //
-// One CTA per SM (persistent), 6 warps:
+// Persistent, one CTA per SM, 6 warps:
 //   warp 0      TMA producer (one elected lane): fills a ring of shared-memory
-//               stages with 128x64 A and 256x64 B bf16 tiles (128-byte swizzle)
-//   warp 1      TMEM allocator, then MMA issuer (one elected lane):
-//               tcgen05.mma 128x256x16, fp32 accumulator in TMEM, two
-//               accumulator buffers (2 x 256 columns = all 512 columns) so the
-//               epilogue of tile t overlaps the main loop of tile t+1
-//   warps 2..5  epilogue: warp w reads TMEM lanes 32*(w%4) .. +31, i.e. each
-//               thread owns one row of the 128-row tile
+//               stages with bf16 operand tiles (128-byte swizzle)
+//   warp 1      TMEM allocator, then MMA issuer (one elected lane): tcgen05.mma
+//               with a double-buffered fp32 accumulator in TMEM (2 x 256
+//               columns = all 512), so the epilogue of tile t overlaps the main
+//               loop of tile t+1
+//   warps 2..5  epilogue: warp w reads TMEM lanes 32*(w%4) .. +31, so each
+//               thread owns one accumulator row
+//
+// Two tile shapes:
+//   PAIR = false  one CTA computes a 128 x 256 tile (tcgen05.mma.cta_group::1,
+//                 M = 128); a stage holds 128 x 64 of A and 256 x 64 of B.
+//   PAIR = true   a cluster of two CTAs on two SMs computes a 256 x 256 tile
+//                 (tcgen05.mma.cta_group::2, M = 256).  Each CTA loads its own
+//                 128 rows of A and its half (128 rows) of B, so a stage is
+//                 32 KB per SM instead of 48 KB; the leader CTA (rank 0) issues
+//                 the MMAs, which read both CTAs' shared memory and write each
+//                 CTA's 128 accumulator rows into its own TMEM.
 //
 // D = A * B^T with A: M x K and B: N x K as the MMA sees them.  Either operand
 // may be K-major (K contiguous in memory) or MN-major (M/N contiguous):
@@ -39,12 +49,9 @@
 
 namespace flce {
 
-constexpr int BM = 128;                // tile rows (TMEM lanes)
+constexpr int BM = 128;                // accumulator rows per CTA (TMEM lanes)
 constexpr int BN = 256;                // tile columns (TMEM columns per buffer)
 constexpr int BK = 64;                 // bf16 elements per 128-byte row
-constexpr int A_STAGE_BYTES = BM * 128;
-constexpr int B_STAGE_BYTES = BN * 128;
-constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
 constexpr int MN_BOX_BYTES = 64 * 128;  // one MN-major box: 64 MN elements x 64 k rows
 constexpr int NUM_THREADS = 192;
 constexpr int NUM_EPI_WARPS = 4;
@@ -54,13 +61,23 @@ constexpr int TMEM_COLS = 2 * BN;
 constexpr int BARRIER_BYTES = 256;
 constexpr float LOG2E = 1.4426950408889634f;
 
+// Tile geometry of the two variants.
+template <bool PAIR>
+struct TileCfg {
+  static constexpr int TILE_M = PAIR ? 2 * BM : BM;    // rows of D per (pair of) CTA(s)
+  static constexpr int B_ROWS = PAIR ? BN / 2 : BN;    // rows of B this CTA loads
+  static constexpr int A_STAGE = BM * 128;             // bytes of A per stage
+  static constexpr int B_STAGE = B_ROWS * 128;         // bytes of B per stage
+  static constexpr int STAGE = A_STAGE + B_STAGE;
+};
+
 enum class Epi : int { kLse = 0, kDz = 1, kStore = 2 };
 
 struct GemmParams {
   int m_size;      // rows of D
   int n_size;      // columns of D
   int k_size;      // contraction length
-  int m_blocks;    // ceil(m_size / BM)
+  int m_blocks;    // ceil(m_size / TILE_M)
   int n_blocks;    // ceil(n_size / BN)
   int group_len;   // consecutive column tiles per work unit
   int n_groups;    // ceil(n_blocks / group_len)
@@ -74,7 +91,7 @@ struct GemmParams {
   int col_limit;          // D columns >= col_limit do not exist
   float smoothing;        // eps
   float4* partials;       // kLse: [n_groups][m_pad] of (max*log2e, sum, z_y, sum_z)
-  int m_pad;              // m_blocks * BM
+  int m_pad;              // m_blocks * TILE_M
   const float* lse;       // kDz: per-row log-sum-exp
   const float* scale;     // kDz: device scalar c = grad / N_valid
   // kStore
@@ -84,9 +101,10 @@ struct GemmParams {
   unsigned long long timeout_ns;
 };
 
-template <Epi EPI, int STAGES>
+template <Epi EPI, int STAGES, bool PAIR>
 constexpr int gemm_smem_bytes() {
-  return STAGES * STAGE_BYTES + (EPI == Epi::kLse ? 0 : STAGING_BYTES) + BARRIER_BYTES + 1024;
+  return STAGES * TileCfg<PAIR>::STAGE + (EPI == Epi::kLse ? 0 : STAGING_BYTES) + BARRIER_BYTES +
+         1024;
 }
 
 __device__ __forceinline__ void unit_coords(const GemmParams& p, int u, int& mb, int& nb0,
@@ -136,16 +154,16 @@ __device__ __forceinline__ void staging_write_row(uint32_t buf, int row, const u
   }
 }
 
-template <Epi EPI, bool A_MN, bool B_MN, int STAGES>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ CUtensorMap tmOut, const GemmParams p) {
+template <Epi EPI, bool A_MN, bool B_MN, int STAGES, bool PAIR>
+__device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensorMap& tmB,
+                                          const CUtensorMap& tmOut, const GemmParams& p) {
+  using Cfg = TileCfg<PAIR>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* stages = smem;
   constexpr int kStaging = (EPI == Epi::kLse) ? 0 : STAGING_BYTES;
-  uint8_t* staging = smem + STAGES * STAGE_BYTES;
+  uint8_t* staging = smem + STAGES * Cfg::STAGE;
   uint64_t* full = reinterpret_cast<uint64_t*>(staging + kStaging);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
@@ -156,6 +174,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;  // 0 = leader (issues the MMAs)
+  const int pair_id = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int num_pairs = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -164,7 +185,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], NUM_EPI_WARPS);
+      mbar_init(&tempty[a], PAIR ? 2 * NUM_EPI_WARPS : NUM_EPI_WARPS);
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -176,11 +197,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (EPI != Epi::kLse) prefetch_tensormap(&tmOut);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(tmem_slot, TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR) {
+    cluster_sync_all();  // the peer's barriers exist before any remote arrive
+  } else {
+    __syncthreads();
+  }
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const WaitCtx ctx{abort_flag, p.err_word, p.timeout_ns};
@@ -191,10 +221,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+      for (int u = pair_id; u < p.num_units && ok; u += num_pairs) {
         int mb, nb0, nb1, g;
         unit_coords(p, u, mb, nb0, nb1, g);
+        const int a_row = mb * Cfg::TILE_M + (int)rank * BM;
         for (int nb = nb0; nb < nb1 && ok; ++nb) {
+          const int b_row = nb * BN + (int)rank * Cfg::B_ROWS;
           for (int kb = 0; kb < num_kb; ++kb) {
             const int s = it % STAGES;
             const uint32_t r = it / STAGES;
@@ -202,28 +234,49 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               ok = false;
               break;
             }
-            uint8_t* a_dst = stages + s * STAGE_BYTES;
-            uint8_t* b_dst = a_dst + A_STAGE_BYTES;
-            mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
-            if constexpr (!A_MN) {
-              tma_load_2d(a_dst, &tmA, &full[s], kb * BK, mb * BM);
-            } else {
+            uint8_t* a_dst = stages + s * Cfg::STAGE;
+            uint8_t* b_dst = a_dst + Cfg::A_STAGE;
+            if constexpr (PAIR) {
+              // Both CTAs' loads complete on the leader's full barrier, which
+              // only the leader arms with the pair's byte count.
+              const uint32_t bar = mapa_shared(smem_u32(&full[s]), 0);
+              if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * Cfg::STAGE);
+              if constexpr (!A_MN) {
+                tma_load_2d_pair(a_dst, &tmA, bar, kb * BK, a_row);
+              } else {
 #pragma unroll
-              for (int i = 0; i < BM / 64; ++i)
-                tma_load_2d(a_dst + i * MN_BOX_BYTES, &tmA, &full[s], mb * BM + i * 64, kb * BK);
-            }
-            if constexpr (!B_MN) {
-              tma_load_2d(b_dst, &tmB, &full[s], kb * BK, nb * BN);
-            } else {
+                for (int i = 0; i < BM / 64; ++i)
+                  tma_load_2d_pair(a_dst + i * MN_BOX_BYTES, &tmA, bar, a_row + i * 64, kb * BK);
+              }
+              if constexpr (!B_MN) {
+                tma_load_2d_pair(b_dst, &tmB, bar, kb * BK, b_row);
+              } else {
 #pragma unroll
-              for (int i = 0; i < BN / 64; ++i)
-                tma_load_2d(b_dst + i * MN_BOX_BYTES, &tmB, &full[s], nb * BN + i * 64, kb * BK);
+                for (int i = 0; i < Cfg::B_ROWS / 64; ++i)
+                  tma_load_2d_pair(b_dst + i * MN_BOX_BYTES, &tmB, bar, b_row + i * 64, kb * BK);
+              }
+            } else {
+              mbar_arrive_expect_tx(&full[s], Cfg::STAGE);
+              if constexpr (!A_MN) {
+                tma_load_2d(a_dst, &tmA, &full[s], kb * BK, a_row);
+              } else {
+#pragma unroll
+                for (int i = 0; i < BM / 64; ++i)
+                  tma_load_2d(a_dst + i * MN_BOX_BYTES, &tmA, &full[s], a_row + i * 64, kb * BK);
+              }
+              if constexpr (!B_MN) {
+                tma_load_2d(b_dst, &tmB, &full[s], kb * BK, b_row);
+              } else {
+#pragma unroll
+                for (int i = 0; i < Cfg::B_ROWS / 64; ++i)
+                  tma_load_2d(b_dst + i * MN_BOX_BYTES, &tmB, &full[s], b_row + i * 64, kb * BK);
+              }
             }
             ++it;
           }
         }
       }
-      if (!ok) {
+      if (!ok && rank == 0) {
         // Drain: the loads of the last (up to) STAGES issued iterations may
         // still be landing in shared memory.
         const uint32_t first = it > (uint32_t)STAGES ? it - STAGES : 0u;
@@ -233,11 +286,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = make_idesc(false, A_MN, B_MN, BM, BN);
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc = make_idesc(false, A_MN, B_MN, Cfg::TILE_M, BN);
+      // MN-major operand blocks are 64 elements wide; LBO = distance between them.
+      constexpr uint32_t kMnLbo = MN_BOX_BYTES;
       uint32_t it = 0, tile = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+      for (int u = pair_id; u < p.num_units && ok; u += num_pairs) {
         int mb, nb0, nb1, g;
         unit_coords(p, u, mb, nb0, nb1, g);
         for (int nb = nb0; nb < nb1 && ok; ++nb) {
@@ -257,32 +312,44 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               break;
             }
             tc_fence_after();
-            const uint32_t a_addr = smem_u32(stages + s * STAGE_BYTES);
-            const uint32_t b_addr = a_addr + A_STAGE_BYTES;
+            const uint32_t a_addr = smem_u32(stages + s * Cfg::STAGE);
+            const uint32_t b_addr = a_addr + Cfg::A_STAGE;
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk) {
-              const uint64_t ad = A_MN ? smem_desc_sw128(a_addr + kk * 2048, MN_BOX_BYTES, 1024)
+              const uint64_t ad = A_MN ? smem_desc_sw128(a_addr + kk * 2048, kMnLbo, 1024)
                                        : smem_desc_sw128(a_addr + kk * 32, 16, 1024);
-              const uint64_t bd = B_MN ? smem_desc_sw128(b_addr + kk * 2048, MN_BOX_BYTES, 1024)
+              const uint64_t bd = B_MN ? smem_desc_sw128(b_addr + kk * 2048, kMnLbo, 1024)
                                        : smem_desc_sw128(b_addr + kk * 32, 16, 1024);
-              mma_issue<false>(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+              if constexpr (PAIR)
+                mma_issue_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+              else
+                mma_issue<false>(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
             }
-            mma_commit(&empty[s]);
+            if constexpr (PAIR)
+              mma_commit_pair_multicast(&empty[s], 0x3);
+            else
+              mma_commit(&empty[s]);
             ++it;
           }
           if (!ok) break;
-          mma_commit(&tfull[acc]);
+          if constexpr (PAIR)
+            mma_commit_pair_multicast(&tfull[acc], 0x3);
+          else
+            mma_commit(&tfull[acc]);
           ++tile;
         }
       }
       // Every MMA this thread issued must finish before TMEM is released.
-      mma_commit(mma_done);
+      if constexpr (PAIR)
+        mma_commit_pair_multicast(mma_done, 0x1);
+      else
+        mma_commit(mma_done);
       mbar_wait_drain(mma_done, 0, p.timeout_ns);
     }
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;              // TMEM lane quadrant of this warp
-    const int row_in_tile = q * 32 + lane;
+    const int row_in_tile = (int)rank * BM + q * 32 + lane;
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     const uint32_t stag0 = smem_u32(staging) + (warp - 2) * 2 * STAGING_BUF_BYTES;
     uint32_t tile = 0;
@@ -290,15 +357,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     float c_scale = 0.f;
     if constexpr (EPI == Epi::kDz) c_scale = *p.scale;
 
-    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+    for (int u = pair_id; u < p.num_units && ok; u += num_pairs) {
       int mb, nb0, nb1, g;
       unit_coords(p, u, mb, nb0, nb1, g);
-      const int row = mb * BM + row_in_tile;
+      const int row = mb * Cfg::TILE_M + row_in_tile;
+      const int store_row0 = mb * Cfg::TILE_M + (int)rank * BM + q * 32;
       const bool row_ok = row < p.m_size;
 
       // Per-row state for kLse (natural-log max is m2 / log2(e)).
       float m2 = -INFINITY, ssum = 0.f, zy = 0.f, zsum = 0.f;
-      long long label = row_ok ? (long long)p.labels[row] : (long long)p.ignore_index;
+      long long label = 0;
+      if constexpr (EPI != Epi::kStore)
+        label = row_ok ? (long long)p.labels[row] : (long long)p.ignore_index;
       const bool valid = row_ok && label != p.ignore_index;
       const long long lab_rel = label - p.col_base;
 
@@ -352,12 +422,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               for (int j = 0; j < 32; ++j) zs += (j < nvalid) ? __uint_as_float(r[j]) : 0.f;
               zsum += zs;
             }
+            // target logit: a select chain (no dynamic register indexing)
             const long long off = lab_rel - c0;
-            if (off >= 0 && off < 32 && off < nvalid) {
+            const int offi = (off >= 0 && off < 32 && off < nvalid) ? (int)off : -1;
 #pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (j == (int)off) zy = __uint_as_float(r[j]);
-            }
+            for (int j = 0; j < 32; ++j) zy = (j == offi) ? __uint_as_float(r[j]) : zy;
           }
         } else if constexpr (EPI == Epi::kDz) {
 #pragma unroll 1
@@ -394,7 +463,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             fence_proxy_async_shared();
             __syncwarp();
             if (lane == 0) {
-              tma_store_2d(&tmOut, staging + (buf - smem_u32(staging)), c0, mb * BM + q * 32);
+              tma_store_2d(&tmOut, staging + (buf - smem_u32(staging)), c0, store_row0);
               bulk_commit_group();
             }
           }
@@ -415,18 +484,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (lane == 0) {
               const void* src = staging + (buf - smem_u32(staging));
               if (p.reduce_add)
-                tma_reduce_add_2d(&tmOut, src, c0, mb * BM + q * 32);
+                tma_reduce_add_2d(&tmOut, src, c0, store_row0);
               else
-                tma_store_2d(&tmOut, src, c0, mb * BM + q * 32);
+                tma_store_2d(&tmOut, src, c0, store_row0);
               bulk_commit_group();
             }
           }
         }
 
-        // Release the accumulator buffer to the MMA warp.
+        // Release the accumulator buffer to the MMA warp (the leader's barrier).
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[acc]);
+        if (lane == 0) {
+          if constexpr (PAIR)
+            mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
+          else
+            mbar_arrive(&tempty[acc]);
+        }
         ++tile;
       }
 
@@ -441,10 +515,41 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 
   __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+  if constexpr (PAIR) {
+    if (*abort_flag) {
+      // After an abort the peer's loads into this CTA may still be landing
+      // (they signal the leader's barrier, which this CTA cannot wait on).
+      const uint64_t t0 = global_timer_ns();
+      while (global_timer_ns() - t0 < 200000ull) {
+      }
+    }
+    tc_fence_before();
+    cluster_sync_all();  // all pair MMAs and remote arrivals are done
+    if (warp == 1) {
+      tc_fence_after();
+      tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    }
+  } else {
+    if (warp == 1) {
+      tc_fence_after();
+      tmem_dealloc(tmem_base, TMEM_COLS);
+    }
   }
+}
+
+template <Epi EPI, bool A_MN, bool B_MN, int STAGES>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmOut, const GemmParams p) {
+  gemm_body<EPI, A_MN, B_MN, STAGES, false>(tmA, tmB, tmOut, p);
+}
+
+template <Epi EPI, bool A_MN, bool B_MN, int STAGES>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmOut, const GemmParams p) {
+  gemm_body<EPI, A_MN, B_MN, STAGES, true>(tmA, tmB, tmOut, p);
 }
 
 }  // namespace flce

@@ -2,8 +2,9 @@
 
 D = A B^T for every operand layout the loss path uses: K-major A and B (the
 logit GEMM), MN-major A and B (the dW GEMM), K-major A with MN-major B (the dX
-GEMM), plus MN-major A with K-major B.  Checked against a float64 product of
-the same bf16 values.
+GEMM), plus MN-major A with K-major B, for both tile shapes (CTA-pair 256 x 256 and
+single-CTA 128 x 256).  Checked against a float64 product of the same bf16
+values.
 """
 import numpy as np
 import pytest
@@ -15,6 +16,14 @@ SHAPES = [
     (304, 520, 200),    # ragged M, N and K tails
     (1024, 768, 1024),  # several tiles per CTA, long K
 ]
+
+
+@pytest.fixture(params=[1, 0], ids=["cta_pair", "single_cta"], autouse=True)
+def tile_shape(request):
+    from linear_cross_entropy_logit_gb300 import binding as B
+    B.flce_set_cta_pair(request.param)
+    yield request.param
+    B.flce_set_cta_pair(1)
 
 
 def _bf16(rng, shape):

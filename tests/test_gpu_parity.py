@@ -22,8 +22,10 @@ pytestmark = pytest.mark.gpu
 def _auto_chunk():
     from linear_cross_entropy_logit_gb300 import binding as B
     B.flce_set_vocab_chunk(0)
+    B.flce_set_cta_pair(1)
     yield
     B.flce_set_vocab_chunk(0)
+    B.flce_set_cta_pair(1)
 
 
 def run_fwd_bwd(wl, reduction="mean", grad=None, chunk=0, dW0=None):
@@ -65,11 +67,27 @@ def test_tiny_config_fp32():
     check_against_oracle(wl, run_fwd_bwd(wl))
 
 
+@pytest.mark.parametrize("pair", [1, 0], ids=["cta_pair", "single_cta"])
 @pytest.mark.parametrize("chunk", [0, 256, 512])
-def test_ragged_multi_tile(chunk):
+def test_ragged_multi_tile(chunk, pair):
     # 3 row blocks (last ragged), 4 vocabulary tiles (last ragged), K tail of 8
+    from linear_cross_entropy_logit_gb300 import binding as B
+    B.flce_set_cta_pair(pair)
     wl = I.make_workload(spec(N=300, H=136, V=1000, n_ignore=30, smoothing=0.1), seed=1)
     check_against_oracle(wl, run_fwd_bwd(wl, chunk=chunk))
+
+
+def test_tile_shapes_agree():
+    """CTA-pair and single-CTA tiles give the same results up to fp32 summation order."""
+    from linear_cross_entropy_logit_gb300 import binding as B
+    wl = I.make_workload(spec(N=700, H=264, V=3000, n_ignore=50, smoothing=0.1), seed=15)
+    B.flce_set_cta_pair(1)
+    a = run_fwd_bwd(wl)
+    B.flce_set_cta_pair(0)
+    b = run_fwd_bwd(wl)
+    assert rel_err(a["loss"], b["loss"]) <= 1e-5
+    assert np.max(np.abs(a["lse"] - b["lse"])) <= 1e-4
+    assert rel_fro(a["dX"], b["dX"]) <= 5e-3 and rel_fro(a["dW"], b["dW"]) <= 5e-3
 
 
 def test_sum_reduction_with_upstream_grad():

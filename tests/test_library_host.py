@@ -36,7 +36,7 @@ def test_header_exports_all(L):
 
 
 def test_status_strings_and_version(L):
-    assert L.flce_abi_version() == 100
+    assert L.flce_abi_version() == 101
     for s in range(7):
         assert L.flce_status_string(s).decode().startswith("FLCE_")
 
