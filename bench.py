@@ -50,6 +50,10 @@ def parse_args():
     ap.add_argument("--reference-rows", type=int, default=128,
                     help="token rows per oracle step of --impl reference")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--l2-hints", action="store_true",
+                    help="evict_last L2 policy for the operand re-read on every wave of tiles")
+    ap.add_argument("--single-cta", action="store_true",
+                    help="128x256 single-CTA tiles instead of 256x256 CTA-pair tiles")
     return ap.parse_args()
 
 
@@ -216,6 +220,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     wl = I.make_workload(spec, seed=args.seed + rank)
     N, H, V = spec.N, spec.H, spec.V
     B.flce_set_vocab_chunk(args.vocab_chunk)
+    B.flce_set_l2_hints(args.l2_hints)
+    B.flce_set_cta_pair(not args.single_cta)
     chunk = B.flce_vocab_chunk(N, V)
 
     def host_tensor(a):
@@ -286,45 +292,78 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     tokens_per_s = world * N * args.steps / (ms / 1e3)
 
     # --- end-to-end through the C ABI with host buffers --------------------
+    # Every step copies its inputs (X, W, labels) from pinned host memory and
+    # its outputs (loss, lse, dX, dW) back.  Device buffers are double-buffered
+    # so that step k+1's upload and step k-1's download overlap step k's fused
+    # call (three streams ordered by events); the timed region runs from the
+    # first upload to the last download.
     e2e = None
     if not args.no_e2e:
         Xp, Wp, yp = Xh.pin_memory(), Wh.pin_memory(), yh.pin_memory()
-        loss_h = torch.empty(1, dtype=torch.float32).pin_memory()
-        lse_h = torch.empty(N, dtype=torch.float32).pin_memory()
-        dX_h = torch.empty(dX.shape, dtype=dX.dtype).pin_memory()
-        dW_h = torch.empty(dW.shape, dtype=torch.float32).pin_memory()
         h2d = Xp.numel() * Xp.element_size() + Wp.numel() * Wp.element_size() + yp.numel() * 8
-        d2h = 4 + 4 * N + dX_h.numel() * dX_h.element_size() + dW_h.numel() * 4
+        d2h = 4 + 4 * N + dX.numel() * dX.element_size() + dW.numel() * 4
+        slots = []
+        for b in range(2):
+            if b == 0:
+                dev_in = (X, W, y)
+                dev_out = (loss, lse, dX, dW)
+            else:
+                dev_in = (torch.empty_like(X), torch.empty_like(W), torch.empty_like(y))
+                dev_out = (torch.empty_like(loss), torch.empty_like(lse), torch.empty_like(dX),
+                           torch.empty_like(dW))
+            host_out = tuple(torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in dev_out)
+            slots.append({"in": dev_in, "out": dev_out, "host": host_out,
+                          "nv": torch.empty_like(nv),
+                          "ev_in": torch.cuda.Event(), "ev_comp": torch.cuda.Event(),
+                          "ev_out": torch.cuda.Event()})
+        s_up = torch.cuda.Stream(dev)
+        s_down = torch.cuda.Stream(dev)
 
-        def e2e_step():
-            X.copy_(Xp, non_blocking=True)
-            W.copy_(Wp, non_blocking=True)
-            y.copy_(yp, non_blocking=True)
-            step()
-            loss_h.copy_(loss, non_blocking=True)
-            lse_h.copy_(lse, non_blocking=True)
-            dX_h.copy_(dX, non_blocking=True)
-            dW_h.copy_(dW, non_blocking=True)
+        def e2e_step(k):
+            sl = slots[k % 2]
+            xd, wd, yd = sl["in"]
+            with torch.cuda.stream(s_up):
+                s_up.wait_event(sl["ev_comp"])      # step k-2 no longer reads these inputs
+                xd.copy_(Xp, non_blocking=True)
+                wd.copy_(Wp, non_blocking=True)
+                yd.copy_(yp, non_blocking=True)
+                sl["ev_in"].record(s_up)
+            stream.wait_event(sl["ev_in"])
+            stream.wait_event(sl["ev_out"])         # step k-2's outputs are downloaded
+            lo, ls, dx, dw = sl["out"]
+            B.flce_fwd_bwd(xd, wd, yd, spec.ignore_index, spec.smoothing, spec.reduction,
+                           loss=lo, lse=ls, valid_count=sl["nv"], dX=dx, dW=dw,
+                           workspace_buf=ws, err_word=err, stream=stream)
+            sl["ev_comp"].record(stream)
+            with torch.cuda.stream(s_down):
+                s_down.wait_event(sl["ev_comp"])
+                for h, d in zip(sl["host"], sl["out"]):
+                    h.copy_(d, non_blocking=True)
+                sl["ev_out"].record(s_down)
 
-        for _ in range(max(args.warmup, 1)):
-            e2e_step()
+        for k in range(max(args.warmup, 2)):
+            e2e_step(k)
         torch.cuda.synchronize(dev)
         if world > 1:
             dist.barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
-        e1.record(stream)
+        e0.record(s_up)
+        for k in range(args.steps):
+            e2e_step(k)
+        e1.record(s_down)
         torch.cuda.synchronize(dev)
         ems = e0.elapsed_time(e1)
         if world > 1:
             t = torch.tensor([ems], device=dev)
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             ems = float(t.item())
+        if int(err.item()) != 0:
+            raise RuntimeError(f"device error word {int(err.item())} in the end-to-end loop")
+        host_loss = float(slots[(args.steps - 1) % 2]["host"][0].item())
         e2e = {"value": world * N * args.steps / (ems / 1e3), "unit": "tokens/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "ms_per_step": ems / args.steps}
+               "ms_per_step": ems / args.steps, "loss_read_back": host_loss,
+               "overlap": "uploads and downloads of neighbouring steps overlap the fused call"}
 
     if rank != 0:
         return
@@ -378,7 +417,9 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "dtype": spec.dtype, "data": "synthetic",
         "config": dict(workload_config(spec, chunk),
                        l2="inputs larger than L2 (W alone is %.2f GB)" % (V * H * elem / 1e9),
-                       parallelism=f"replicas x{world} (each rank its own batch, no collective)"),
+                       parallelism=f"replicas x{world} (each rank its own batch, no collective)",
+                       tiles="128x256 single CTA" if args.single_cta else "256x256 CTA pair",
+                       l2_hints=args.l2_hints),
         "tflops": tflops,
         "step_roofline": {"bound": "tensor" if t_tensor >= t_hbm else "hbm",
                           "frac": step_frac, "flops": flops_step, "bytes": bytes_step,

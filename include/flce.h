@@ -97,6 +97,13 @@ int64_t flce_vocab_chunk(int64_t N, int64_t V);
 flce_status flce_set_cta_pair(int on);
 int flce_cta_pair(void);
 
+/* L2 residency hints, process-wide.  1: the operand a GEMM re-reads on every
+ * wave of tiles (X, or a W chunk) is loaded with an evict_last policy covering
+ * up to ~64 MB of L2.  0 (the default; on a GB300 the hints did not speed up
+ * the llama3-shaped step and slowed the dW GEMM by ~3%): no hints.  Results do
+ * not depend on it. */
+flce_status flce_set_l2_hints(int on);
+
 /* Forward ("Mathematical Mechanics of Chunked Online Cross-Entropy", steps
  * 1-2): loss (device float, 1), lse (device float, N, every row including
  * ignored ones), valid_count (device int32, 1: N_valid).  workspace: device,

@@ -36,7 +36,7 @@ EXPORTED = (
     "flce_backward", "flce_fwd_bwd", "flce_status_string", "flce_last_cuda_error",
     "flce_last_launch_count", "flce_abi_version", "flce_debug_gemm", "flce_profile_enable",
     "flce_profile_read", "flce_profile_reset", "flce_forward_noalloc", "flce_noalloc_last_error",
-    "flce_set_cta_pair", "flce_cta_pair",
+    "flce_set_cta_pair", "flce_cta_pair", "flce_set_l2_hints",
 )
 
 PROFILE_KINDS = ("fwd_logits_lse", "bwd_dz_recompute", "bwd_dw_gemm", "bwd_dx_gemm")
@@ -102,6 +102,8 @@ def lib() -> ctypes.CDLL:
     L.flce_set_cta_pair.restype = I32
     L.flce_cta_pair.argtypes = []
     L.flce_cta_pair.restype = I32
+    L.flce_set_l2_hints.argtypes = [I32]
+    L.flce_set_l2_hints.restype = I32
     _lib = L
     return L
 
@@ -163,6 +165,10 @@ def flce_set_vocab_chunk(cols: int) -> None:
 def flce_set_cta_pair(on: bool) -> None:
     """1: 256 x 256 tiles on CTA pairs (default); 0: 128 x 256 tiles on single CTAs."""
     _check(lib().flce_set_cta_pair(int(bool(on))), "flce_set_cta_pair")
+
+
+def flce_set_l2_hints(on: bool) -> None:
+    _check(lib().flce_set_l2_hints(int(bool(on))), "flce_set_l2_hints")
 
 
 def flce_cta_pair() -> bool:

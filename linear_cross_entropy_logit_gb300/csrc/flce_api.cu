@@ -325,6 +325,14 @@ flce_status launch_tile(bool pair, int dev, int num_sms, const CUtensorMap& a,
 }
 
 bool use_pair() { return g_cta_pair.load() != 0; }
+
+// Fraction of the reused operand's lines kept in L2 with evict_last priority:
+// about 64 MB of the 129 MB L2 is given to it, the rest streams.
+std::atomic<int> g_l2_hints{0};
+float l2_keep_fraction(double operand_bytes) {
+  if (!g_l2_hints.load() || operand_bytes <= 0) return 0.f;
+  return (float)std::min(1.0, (64.0 * (1 << 20)) / operand_bytes);
+}
 int tile_rows(bool pair) { return pair ? 2 * BM : BM; }
 uint32_t b_box_rows(bool pair) { return pair ? BN / 2 : BN; }
 
@@ -422,6 +430,8 @@ flce_status run_forward(const Common& c, const Plan& pl, int dev, int sms, const
     p.smoothing = c.smoothing;
     p.partials = reinterpret_cast<float4*>(ws + pl.off_partials);
     p.m_pad = pl.m_pad;
+    p.l2_keep_b = 0;
+    p.l2_keep_frac = l2_keep_fraction((double)c.N * c.H * 2);
     p.err_word = c.err_word;
     p.timeout_ns = kTimeoutNs;
     FLCE_TRY((launch_tile<Epi::kLse, false, false>(pair, dev, sms, tmX, tmW, tmX, p, c.st, 0)));
@@ -496,6 +506,8 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
     p3.smoothing = c.smoothing;
     p3.lse = lse;
     p3.scale = scale;
+    p3.l2_keep_b = 0;  // X is reused by every wave; the W tile is shared within one
+    p3.l2_keep_frac = l2_keep_fraction((double)N * H * 2);
     p3.err_word = c.err_word;
     p3.timeout_ns = kTimeoutNs;
     FLCE_TRY((launch_tile<Epi::kDz, false, false>(pair, dev, sms, tmX_k, tmWc_k, tmDzSt, p3, c.st, 1)));
@@ -512,6 +524,8 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
     p4.num_units = p4.m_blocks * h_blocks;
     p4.m_fastest = 0;
     p4.reduce_add = accumulate ? 1 : 0;
+    p4.l2_keep_b = 1;  // X again; the dZ column block is shared within one wave
+    p4.l2_keep_frac = l2_keep_fraction((double)N * H * 2);
     p4.err_word = c.err_word;
     p4.timeout_ns = kTimeoutNs;
     FLCE_TRY((launch_tile<Epi::kStore, true, true>(pair, dev, sms, tmDz_mn, tmX_mn, tmDw, p4, c.st, 2)));
@@ -528,6 +542,8 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
     p5.num_units = m_blocks_tok * h_blocks;
     p5.m_fastest = 0;
     p5.reduce_add = ci > 0 ? 1 : 0;
+    p5.l2_keep_b = 1;  // the W chunk; the dZ row block is shared within one wave
+    p5.l2_keep_frac = l2_keep_fraction((double)w * H * 2);
     p5.err_word = c.err_word;
     p5.timeout_ns = kTimeoutNs;
     FLCE_TRY((launch_tile<Epi::kStore, false, true>(pair, dev, sms, tmDz_k, tmWc_mn, tmDxAcc, p5, c.st, 3)));
@@ -601,6 +617,11 @@ void flce_profile_reset(void) {
     g_prof_ms[k] = 0.0;
     g_prof_n[k] = 0;
   }
+}
+
+flce_status flce_set_l2_hints(int on) {
+  g_l2_hints.store(on != 0 ? 1 : 0);
+  return FLCE_OK;
 }
 
 flce_status flce_set_cta_pair(int on) {

@@ -96,6 +96,10 @@ struct GemmParams {
   const float* scale;     // kDz: device scalar c = grad / N_valid
   // kStore
   int reduce_add;         // 1: TMA reduce-add onto the output, 0: overwrite
+  // L2 residency: the operand reused across waves of tiles (0 = A, 1 = B) is
+  // loaded with an evict_last policy covering `l2_keep_frac` of its lines.
+  int l2_keep_b;
+  float l2_keep_frac;
   // control
   int* err_word;
   unsigned long long timeout_ns;
@@ -221,6 +225,9 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
+      const uint64_t keep = l2_policy_evict_last(p.l2_keep_frac);
+      const bool keep_a = p.l2_keep_frac > 0.f && !p.l2_keep_b;
+      const bool keep_b = p.l2_keep_frac > 0.f && p.l2_keep_b;
       for (int u = pair_id; u < p.num_units && ok; u += num_pairs) {
         int mb, nb0, nb1, g;
         unit_coords(p, u, mb, nb0, nb1, g);
@@ -241,35 +248,47 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
               // only the leader arms with the pair's byte count.
               const uint32_t bar = mapa_shared(smem_u32(&full[s]), 0);
               if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * Cfg::STAGE);
+              auto ld = [&](void* dst, const CUtensorMap* m, int x, int y, bool hint) {
+                if (hint)
+                  tma_load_2d_pair_hint(dst, m, bar, x, y, keep);
+                else
+                  tma_load_2d_pair(dst, m, bar, x, y);
+              };
               if constexpr (!A_MN) {
-                tma_load_2d_pair(a_dst, &tmA, bar, kb * BK, a_row);
+                ld(a_dst, &tmA, kb * BK, a_row, keep_a);
               } else {
 #pragma unroll
                 for (int i = 0; i < BM / 64; ++i)
-                  tma_load_2d_pair(a_dst + i * MN_BOX_BYTES, &tmA, bar, a_row + i * 64, kb * BK);
+                  ld(a_dst + i * MN_BOX_BYTES, &tmA, a_row + i * 64, kb * BK, keep_a);
               }
               if constexpr (!B_MN) {
-                tma_load_2d_pair(b_dst, &tmB, bar, kb * BK, b_row);
+                ld(b_dst, &tmB, kb * BK, b_row, keep_b);
               } else {
 #pragma unroll
                 for (int i = 0; i < Cfg::B_ROWS / 64; ++i)
-                  tma_load_2d_pair(b_dst + i * MN_BOX_BYTES, &tmB, bar, b_row + i * 64, kb * BK);
+                  ld(b_dst + i * MN_BOX_BYTES, &tmB, b_row + i * 64, kb * BK, keep_b);
               }
             } else {
               mbar_arrive_expect_tx(&full[s], Cfg::STAGE);
+              auto ld = [&](void* dst, const CUtensorMap* m, int x, int y, bool hint) {
+                if (hint)
+                  tma_load_2d_hint(dst, m, &full[s], x, y, keep);
+                else
+                  tma_load_2d(dst, m, &full[s], x, y);
+              };
               if constexpr (!A_MN) {
-                tma_load_2d(a_dst, &tmA, &full[s], kb * BK, a_row);
+                ld(a_dst, &tmA, kb * BK, a_row, keep_a);
               } else {
 #pragma unroll
                 for (int i = 0; i < BM / 64; ++i)
-                  tma_load_2d(a_dst + i * MN_BOX_BYTES, &tmA, &full[s], a_row + i * 64, kb * BK);
+                  ld(a_dst + i * MN_BOX_BYTES, &tmA, a_row + i * 64, kb * BK, keep_a);
               }
               if constexpr (!B_MN) {
-                tma_load_2d(b_dst, &tmB, &full[s], kb * BK, b_row);
+                ld(b_dst, &tmB, kb * BK, b_row, keep_b);
               } else {
 #pragma unroll
                 for (int i = 0; i < Cfg::B_ROWS / 64; ++i)
-                  tma_load_2d(b_dst + i * MN_BOX_BYTES, &tmB, &full[s], b_row + i * 64, kb * BK);
+                  ld(b_dst + i * MN_BOX_BYTES, &tmB, b_row + i * 64, kb * BK, keep_b);
               }
             }
             ++it;

@@ -226,3 +226,18 @@ def test_autograd_wrapper():
     assert rel_err(loss.item(), f.loss) <= LOSS_REL
     assert rel_fro(tensor_f64(X.grad), b.dX) <= GRAD_REL_FRO
     assert rel_fro(tensor_f64(W.grad), b.dW) <= GRAD_REL_FRO
+
+
+def test_l2_hints_do_not_change_results():
+    from linear_cross_entropy_logit_gb300 import binding as B
+    wl = I.make_workload(spec(N=640, H=256, V=4000, n_ignore=30, smoothing=0.1), seed=16)
+    try:
+        B.flce_set_l2_hints(True)
+        a = run_fwd_bwd(wl)
+        B.flce_set_l2_hints(False)
+        b = run_fwd_bwd(wl)
+    finally:
+        B.flce_set_l2_hints(False)
+    assert a["loss"] == b["loss"]
+    for k in ("lse", "dX", "dW"):
+        assert np.array_equal(a[k], b[k])
