@@ -40,6 +40,11 @@ notes):
   R8 dW is overwritten unless an accumulator is passed (then +=).
   R11 dlogits = c * (softmax - onehot), c = grad_loss / N_v (mean) or
       grad_loss (sum).
+  R19 z-loss ([CFCE] "Numerical Considerations ...", item 3, gives
+      L_z = alpha * log^2 sum_j exp(z_ij) per token without saying how it is
+      averaged): each valid token adds alpha * lse_i^2 to its loss, averaged
+      with the same normaliser as the cross-entropy; its gradient adds
+      c * 2 alpha lse_i * softmax_ij to dZ_ij.
 
 Rows are independent in every formula below.  ``forward`` therefore walks
 the rows in groups only to bound memory; no value is computed differently
@@ -115,16 +120,18 @@ def grad_scale(n_valid: int, reduction: str, grad_loss: float = 1.0) -> float:
 
 
 def row_losses(Z: np.ndarray, lse: np.ndarray, labels: np.ndarray,
-               valid: np.ndarray, smoothing: float) -> np.ndarray:
-    """l_i = valid_i * (lse_i - (1-eps) z_{i,y_i} - (eps/V) sum_j z_ij)   (R1).
-
-    With eps = 0 this is [CFCE] step 2's l_i = -z_{i,y_i} + m_i + log d_i."""
+               valid: np.ndarray, smoothing: float, z_loss: float = 0.0) -> np.ndarray:
+    """l_i = valid_i * (lse_i - (1-eps) z_{i,y_i} - (eps/V) sum_j z_ij + alpha lse_i^2)
+    (R1, R19).  With eps = alpha = 0 this is [CFCE] step 2's
+    l_i = -z_{i,y_i} + m_i + log d_i."""
     V = Z.shape[1]
     y = np.where(valid, labels, 0)
     z_y = Z[np.arange(Z.shape[0]), y]
     loss = lse - (1.0 - smoothing) * z_y
     if smoothing != 0.0:
         loss = loss - (smoothing / V) * Z.sum(axis=1)
+    if z_loss != 0.0:
+        loss = loss + z_loss * lse * lse
     return np.where(valid, loss, 0.0)
 
 
@@ -140,7 +147,7 @@ class ForwardResult:
 
 def forward(X, W, labels, ignore_index: int = IGNORE_INDEX,
             smoothing: float = 0.0, reduction: str = "mean",
-            row_group: int = 512) -> ForwardResult:
+            row_group: int = 512, z_loss: float = 0.0) -> ForwardResult:
     """Loss, per-row lse and per-row loss ([CFCE] steps 1-2, [CCE] loss)."""
     Xd, Wd = upcast(X), upcast(W)
     N, V = Xd.shape[0], Wd.shape[0]
@@ -153,7 +160,8 @@ def forward(X, W, labels, ignore_index: int = IGNORE_INDEX,
         r1 = min(N, r0 + row_group)
         Z = Xd[r0:r1] @ Wd.T
         m[r0:r1], _, lse[r0:r1] = row_logsumexp(Z)
-        row_loss[r0:r1] = row_losses(Z, lse[r0:r1], labels[r0:r1], valid[r0:r1], smoothing)
+        row_loss[r0:r1] = row_losses(Z, lse[r0:r1], labels[r0:r1], valid[r0:r1], smoothing,
+                                     z_loss)
     n_valid = int(valid.sum())
     loss_sum = float(row_loss.sum())
     if reduction == "mean":
@@ -170,9 +178,13 @@ def forward(X, W, labels, ignore_index: int = IGNORE_INDEX,
 #   dZ_ij = c * valid_i * (exp(z_ij - lse_i) - (1-eps) 1[j=y_i] - eps/V)
 # ----------------------------------------------------------------------------
 def dlogits(Z: np.ndarray, lse: np.ndarray, labels: np.ndarray,
-            valid: np.ndarray, c: float, smoothing: float) -> np.ndarray:
+            valid: np.ndarray, c: float, smoothing: float,
+            z_loss: float = 0.0) -> np.ndarray:
+    """... + c * valid_i * 2 alpha lse_i * softmax_ij with z-loss (R19)."""
     V = Z.shape[1]
     P = np.exp(Z - lse[:, None])
+    if z_loss != 0.0:
+        P = P * (1.0 + 2.0 * z_loss * lse)[:, None]
     dZ = P - smoothing / V
     rows = np.flatnonzero(valid)
     dZ[rows, labels[rows]] -= (1.0 - smoothing)
@@ -189,7 +201,7 @@ class BackwardResult:
 def backward(X, W, labels, ignore_index: int = IGNORE_INDEX,
              smoothing: float = 0.0, reduction: str = "mean",
              grad_loss: float = 1.0, dW_in: Optional[np.ndarray] = None,
-             n_valid: Optional[int] = None) -> BackwardResult:
+             n_valid: Optional[int] = None, z_loss: float = 0.0) -> BackwardResult:
     """[CFCE] step 4: dX = dZ W and dW = dZ^T X (+ dW_in when accumulating).
 
     ``n_valid`` overrides the local count of valid rows (a data-parallel shard
@@ -202,7 +214,7 @@ def backward(X, W, labels, ignore_index: int = IGNORE_INDEX,
     c = grad_scale(nv, reduction, grad_loss)
     Z = Xd @ Wd.T
     _, _, lse = row_logsumexp(Z)
-    dZ = dlogits(Z, lse, labels, valid, c, smoothing)
+    dZ = dlogits(Z, lse, labels, valid, c, smoothing, z_loss)
     dX = dZ @ Wd
     dW = dZ.T @ Xd
     if dW_in is not None:
@@ -215,7 +227,7 @@ def backward(X, W, labels, ignore_index: int = IGNORE_INDEX,
 # definitions evaluated only where asked.
 # ----------------------------------------------------------------------------
 def forward_rows(X, W, labels, rows: Sequence[int], ignore_index: int = IGNORE_INDEX,
-                 smoothing: float = 0.0):
+                 smoothing: float = 0.0, z_loss: float = 0.0):
     """(lse, row_loss, m) of the selected token rows."""
     rows = np.asarray(rows, dtype=np.int64)
     Wd = upcast(W)
@@ -224,11 +236,12 @@ def forward_rows(X, W, labels, rows: Sequence[int], ignore_index: int = IGNORE_I
     valid = valid_mask(lab, V, ignore_index)
     Z = upcast(np.asarray(X)[rows]) @ Wd.T
     m, _, lse = row_logsumexp(Z)
-    return lse, row_losses(Z, lse, lab, valid, smoothing), m
+    return lse, row_losses(Z, lse, lab, valid, smoothing, z_loss), m
 
 
 def dx_rows(X, W, labels, rows: Sequence[int], c: float,
-            ignore_index: int = IGNORE_INDEX, smoothing: float = 0.0) -> np.ndarray:
+            ignore_index: int = IGNORE_INDEX, smoothing: float = 0.0,
+            z_loss: float = 0.0) -> np.ndarray:
     """dX_i = sum_j dZ_ij W_j for the selected token rows."""
     rows = np.asarray(rows, dtype=np.int64)
     Wd = upcast(W)
@@ -237,11 +250,12 @@ def dx_rows(X, W, labels, rows: Sequence[int], c: float,
     valid = valid_mask(lab, V, ignore_index)
     Z = upcast(np.asarray(X)[rows]) @ Wd.T
     _, _, lse = row_logsumexp(Z)
-    return dlogits(Z, lse, lab, valid, c, smoothing) @ Wd
+    return dlogits(Z, lse, lab, valid, c, smoothing, z_loss) @ Wd
 
 
 def dw_rows(X, W, labels, vocab_rows: Sequence[int], lse: np.ndarray, c: float,
-            ignore_index: int = IGNORE_INDEX, smoothing: float = 0.0) -> np.ndarray:
+            ignore_index: int = IGNORE_INDEX, smoothing: float = 0.0,
+            z_loss: float = 0.0) -> np.ndarray:
     """dW_j = sum_i dZ_ij X_i for the selected vocabulary rows j.
 
     ``lse`` must be the oracle's own lse of every token row (from ``forward``)."""
@@ -252,7 +266,10 @@ def dw_rows(X, W, labels, vocab_rows: Sequence[int], lse: np.ndarray, c: float,
     labels = np.asarray(labels, dtype=np.int64)
     valid = valid_mask(labels, V, ignore_index)
     Zc = Xd @ Wd[vocab_rows].T                   # N x J columns of Z
-    dZc = np.exp(Zc - lse[:, None]) - smoothing / V
+    Pc = np.exp(Zc - lse[:, None])
+    if z_loss != 0.0:
+        Pc = Pc * (1.0 + 2.0 * z_loss * lse)[:, None]
+    dZc = Pc - smoothing / V
     hit = valid[:, None] & (labels[:, None] == vocab_rows[None, :])
     dZc = dZc - (1.0 - smoothing) * hit
     dZc[~valid] = 0.0
@@ -261,8 +278,9 @@ def dw_rows(X, W, labels, vocab_rows: Sequence[int], lse: np.ndarray, c: float,
 
 def fwd_bwd(X, W, labels, ignore_index: int = IGNORE_INDEX, smoothing: float = 0.0,
             reduction: str = "mean", grad_loss: float = 1.0,
-            dW_in: Optional[np.ndarray] = None):
+            dW_in: Optional[np.ndarray] = None, z_loss: float = 0.0):
     """Forward and backward of one batch (what one fused call produces)."""
-    f = forward(X, W, labels, ignore_index, smoothing, reduction)
-    b = backward(X, W, labels, ignore_index, smoothing, reduction, grad_loss, dW_in)
+    f = forward(X, W, labels, ignore_index, smoothing, reduction, z_loss=z_loss)
+    b = backward(X, W, labels, ignore_index, smoothing, reduction, grad_loss, dW_in,
+                 z_loss=z_loss)
     return f, b

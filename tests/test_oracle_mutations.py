@@ -31,6 +31,10 @@ MUTATIONS = [
     ("ignored rows keep gradient", "dZ[~valid] = 0.0", "pass"),
     ("ignored rows keep loss", "return np.where(valid, loss, 0.0)", "return loss"),
     ("dX scaled by a stray factor", "dX = dZ @ Wd", "dX = (dZ @ Wd) * 1.0001"),
+    ("z-loss gradient without the factor 2",
+     "P = P * (1.0 + 2.0 * z_loss * lse)[:, None]", "P = P * (1.0 + z_loss * lse)[:, None]"),
+    ("z-loss term with lse instead of lse^2",
+     "loss = loss + z_loss * lse * lse", "loss = loss + z_loss * lse"),
 ]
 
 

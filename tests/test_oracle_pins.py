@@ -347,3 +347,78 @@ def test_token_shards_compose():
         assert np.allclose(bs.dX, b.dX[p], atol=1e-14)
     assert loss_sum / nv == pytest.approx(f.loss, abs=1e-13)
     assert np.allclose(dW, b.dW, atol=1e-14)
+
+
+# --------------------------------------------------------------------------
+# z-loss (R19): alpha * lse_i^2 per valid token
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("eps", [0.0, 0.1])
+def test_z_loss_zero_weight_closed_form(eps):
+    """W = 0: lse = log V for every row, so loss = log V + alpha log^2 V and
+    dZ_ij = c ((1 + 2 alpha log V)/V - (1-eps) 1[j=y] - eps/V)."""
+    N, H, V, a = 7, 4, 9, 0.03
+    X, _, y = rand_case(N, H, V, 30, n_ignore=2)
+    W = np.zeros((V, H))
+    f = O.forward(X, W, y, IGN, eps, z_loss=a)
+    L = math.log(V)
+    assert f.loss == pytest.approx(L + a * L * L, abs=1e-13)
+    Z = O.logits(X, W)
+    valid = O.valid_mask(y, V, IGN)
+    c = 1.0 / valid.sum()
+    dZ = O.dlogits(Z, f.lse, y, valid, c, eps, a)
+    for i in range(N):
+        for j in range(V):
+            want = 0.0 if y[i] == IGN else c * ((1 + 2 * a * L) / V - eps / V
+                                                - ((1 - eps) if j == y[i] else 0.0))
+            assert dZ[i, j] == pytest.approx(want, abs=1e-15)
+
+
+def test_z_loss_finite_differences():
+    N, H, V, eps, a = 5, 6, 9, 0.1, 0.05
+    X, W, y = rand_case(N, H, V, 31, w_scale=0.5)
+    y[2] = IGN
+    h = 1e-6
+
+    def L(Xa, Wa):
+        return O.forward(Xa, Wa, y, IGN, eps, z_loss=a).loss
+
+    b = O.backward(X, W, y, IGN, eps, z_loss=a)
+    for i in range(N):
+        for k in range(H):
+            Xp, Xm = X.copy(), X.copy()
+            Xp[i, k] += h
+            Xm[i, k] -= h
+            assert abs((L(Xp, W) - L(Xm, W)) / (2 * h) - b.dX[i, k]) <= 1e-7
+    for j in range(V):
+        for k in range(H):
+            Wp, Wm = W.copy(), W.copy()
+            Wp[j, k] += h
+            Wm[j, k] -= h
+            assert abs((L(X, Wp) - L(X, Wm)) / (2 * h) - b.dW[j, k]) <= 1e-7
+
+
+def test_z_loss_against_torch():
+    torch = pytest.importorskip("torch")
+    N, H, V, eps, a = 29, 11, 41, 0.1, 0.02
+    X, W, y = rand_case(N, H, V, 32, n_ignore=5)
+    Xt = torch.tensor(X, requires_grad=True)
+    Wt = torch.tensor(W, requires_grad=True)
+    yt = torch.tensor(y)
+    Z = Xt @ Wt.T
+    valid = yt != IGN
+    ce = torch.nn.functional.cross_entropy(Z, yt, ignore_index=IGN, label_smoothing=eps,
+                                           reduction="sum")
+    zl = (torch.logsumexp(Z, dim=1) ** 2)[valid].sum()
+    loss = (ce + a * zl) / valid.sum()
+    loss.backward()
+    f, b = O.fwd_bwd(X, W, y, IGN, eps, "mean", z_loss=a)
+    assert f.loss == pytest.approx(loss.item(), abs=1e-12)
+    assert np.allclose(b.dX, Xt.grad.numpy(), atol=1e-13)
+    assert np.allclose(b.dW, Wt.grad.numpy(), atol=1e-13)
+    rows = [0, 4, 10]
+    _, rl, _ = O.forward_rows(X, W, y, rows, IGN, eps, z_loss=a)
+    assert np.allclose(rl, f.row_loss[rows], atol=1e-14)
+    c = 1.0 / f.n_valid
+    assert np.allclose(O.dx_rows(X, W, y, rows, c, IGN, eps, a), b.dX[rows], atol=1e-14)
+    assert np.allclose(O.dw_rows(X, W, y, [1, 7], f.lse, c, IGN, eps, a), b.dW[[1, 7]],
+                       atol=1e-14)
