@@ -52,6 +52,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--l2-hints", action="store_true",
                     help="evict_last L2 policy for the operand re-read on every wave of tiles")
+    ap.add_argument("--z-loss", type=float, default=0.0,
+                    help="z-loss weight alpha (adds alpha * lse^2 per valid token)")
     ap.add_argument("--single-cta", action="store_true",
                     help="128x256 single-CTA tiles instead of 256x256 CTA-pair tiles")
     return ap.parse_args()
@@ -248,7 +250,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     def step():
         B.flce_fwd_bwd(X, W, y, spec.ignore_index, spec.smoothing, spec.reduction, loss=loss,
                        lse=lse, valid_count=nv, dX=dX, dW=dW, workspace_buf=ws, err_word=err,
-                       stream=stream)
+                       stream=stream, z_loss=args.z_loss)
         return B.last_launch_count()
 
     for _ in range(max(args.warmup, 0)):
@@ -333,7 +335,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             lo, ls, dx, dw = sl["out"]
             B.flce_fwd_bwd(xd, wd, yd, spec.ignore_index, spec.smoothing, spec.reduction,
                            loss=lo, lse=ls, valid_count=sl["nv"], dX=dx, dW=dw,
-                           workspace_buf=ws, err_word=err, stream=stream)
+                           workspace_buf=ws, err_word=err, stream=stream, z_loss=args.z_loss)
             sl["ev_comp"].record(stream)
             with torch.cuda.stream(s_down):
                 s_down.wait_event(sl["ev_comp"])
@@ -419,6 +421,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                        l2="inputs larger than L2 (W alone is %.2f GB)" % (V * H * elem / 1e9),
                        parallelism=f"replicas x{world} (each rank its own batch, no collective)",
                        tiles="128x256 single CTA" if args.single_cta else "256x256 CTA pair",
+                       z_loss=args.z_loss,
                        l2_hints=args.l2_hints),
         "tflops": tflops,
         "step_roofline": {"bound": "tensor" if t_tensor >= t_hbm else "hbm",

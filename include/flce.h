@@ -137,6 +137,56 @@ flce_status flce_fwd_bwd(const void* X, const void* W, const int64_t* labels, in
                          int accumulate_dW, void* workspace, size_t ws_bytes, int32_t* err_word,
                          void* stream);
 
+/* Options of the extended entry points.  Initialise with
+ * flce_options_init, then set fields:
+ *   ignore_index  labels equal to it are masked (default -100)
+ *   smoothing     label smoothing eps in [0, 1) (default 0)
+ *   z_loss        z-loss weight alpha >= 0 (default 0): each valid token adds
+ *                 alpha * lse_i^2 to its loss ("Chunked and Fused
+ *                 Cross-Entropy ...", "Numerical Considerations and Practical
+ *                 Trade-Offs", item 3: L_z = alpha log^2 sum exp(z)); averaged
+ *                 like the cross-entropy; the gradient gains
+ *                 c * 2 alpha lse_i * softmax_ij
+ *   reduction     FLCE_MEAN or FLCE_SUM (default FLCE_MEAN)
+ *   row_loss      NULL, or a device float[N] that receives every token's loss
+ *                 l_i (0 on ignored rows): the per-token ("none") reduction.
+ *   skip_ignored_blocks
+ *                 0 (default) or 1: skip the projection and the backward GEMMs
+ *                 for blocks of 256 consecutive tokens (128 with
+ *                 flce_set_cta_pair(0)) whose labels are all ignore_index --
+ *                 instruction tuning masks whole prompt spans ("Chunked and
+ *                 Fused Cross-Entropy ...", "Numerical Considerations ...",
+ *                 item 2).  loss, dX and dW are unchanged; lse of the rows of a
+ *                 skipped block is NaN. */
+typedef struct flce_options {
+  size_t struct_size;
+  int64_t ignore_index;
+  float smoothing;
+  float z_loss;
+  flce_reduction reduction;
+  float* row_loss;
+  int skip_ignored_blocks;
+} flce_options;
+
+void flce_options_init(flce_options* opt);
+
+flce_status flce_forward_ex(const void* X, const void* W, const int64_t* labels, int64_t N,
+                            int64_t H, int64_t V, flce_dtype dtype, const flce_options* opt,
+                            float* loss, float* lse, int32_t* valid_count, void* workspace,
+                            size_t ws_bytes, int32_t* err_word, void* stream);
+
+flce_status flce_backward_ex(const void* X, const void* W, const int64_t* labels, int64_t N,
+                             int64_t H, int64_t V, flce_dtype dtype, const flce_options* opt,
+                             const float* lse, const int32_t* valid_count,
+                             const float* grad_loss, void* dX, float* dW, int accumulate_dW,
+                             void* workspace, size_t ws_bytes, int32_t* err_word, void* stream);
+
+flce_status flce_fwd_bwd_ex(const void* X, const void* W, const int64_t* labels, int64_t N,
+                            int64_t H, int64_t V, flce_dtype dtype, const flce_options* opt,
+                            const float* grad_loss, float* loss, float* lse,
+                            int32_t* valid_count, void* dX, float* dW, int accumulate_dW,
+                            void* workspace, size_t ws_bytes, int32_t* err_word, void* stream);
+
 /* Human-readable name of a status code (static string). */
 const char* flce_status_string(flce_status s);
 

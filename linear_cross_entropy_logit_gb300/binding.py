@@ -36,12 +36,21 @@ EXPORTED = (
     "flce_backward", "flce_fwd_bwd", "flce_status_string", "flce_last_cuda_error",
     "flce_last_launch_count", "flce_abi_version", "flce_debug_gemm", "flce_profile_enable",
     "flce_profile_read", "flce_profile_reset", "flce_forward_noalloc", "flce_noalloc_last_error",
-    "flce_set_cta_pair", "flce_cta_pair", "flce_set_l2_hints",
+    "flce_set_cta_pair", "flce_cta_pair", "flce_set_l2_hints", "flce_options_init",
+    "flce_forward_ex", "flce_backward_ex", "flce_fwd_bwd_ex",
 )
 
 PROFILE_KINDS = ("fwd_logits_lse", "bwd_dz_recompute", "bwd_dw_gemm", "bwd_dx_gemm")
 
 _lib = None
+
+
+class FlceOptions(ctypes.Structure):
+    """Mirror of ``flce_options`` in include/flce.h."""
+    _fields_ = [("struct_size", ctypes.c_size_t), ("ignore_index", ctypes.c_int64),
+                ("smoothing", ctypes.c_float), ("z_loss", ctypes.c_float),
+                ("reduction", ctypes.c_int), ("row_loss", ctypes.c_void_p),
+                ("skip_ignored_blocks", ctypes.c_int)]
 
 
 class FlceError(RuntimeError):
@@ -104,6 +113,17 @@ def lib() -> ctypes.CDLL:
     L.flce_cta_pair.restype = I32
     L.flce_set_l2_hints.argtypes = [I32]
     L.flce_set_l2_hints.restype = I32
+    OPT = ctypes.POINTER(FlceOptions)
+    L.flce_options_init.argtypes = [OPT]
+    L.flce_options_init.restype = None
+    L.flce_forward_ex.argtypes = [P, P, P, I64, I64, I64, I32, OPT, P, P, P, P, SZ, P, P]
+    L.flce_forward_ex.restype = I32
+    L.flce_backward_ex.argtypes = [P, P, P, I64, I64, I64, I32, OPT, P, P, P, P, P, I32, P, SZ,
+                                   P, P]
+    L.flce_backward_ex.restype = I32
+    L.flce_fwd_bwd_ex.argtypes = [P, P, P, I64, I64, I64, I32, OPT, P, P, P, P, P, P, I32, P, SZ,
+                                  P, P]
+    L.flce_fwd_bwd_ex.restype = I32
     _lib = L
     return L
 
@@ -189,10 +209,30 @@ def new_err_word(device) -> torch.Tensor:
     return torch.zeros(1, dtype=torch.int32, device=device)
 
 
+def make_options(ignore_index: int = -100, smoothing: float = 0.0, reduction: str = "mean",
+                 z_loss: float = 0.0, row_loss=None, skip_ignored_blocks: bool = False) -> FlceOptions:
+    o = FlceOptions()
+    lib().flce_options_init(ctypes.byref(o))
+    o.ignore_index = ignore_index
+    o.smoothing = smoothing
+    o.z_loss = z_loss
+    o.reduction = _red_code(reduction)
+    o.row_loss = _ptr(row_loss)
+    o.skip_ignored_blocks = int(bool(skip_ignored_blocks))
+    return o
+
+
 def flce_forward(X, W, labels, ignore_index: int = -100, smoothing: float = 0.0,
                  reduction: str = "mean", *, loss=None, lse=None, valid_count=None,
-                 workspace_buf=None, err_word=None, stream=None):
-    """Returns (loss[1] fp32, lse[N] fp32, valid_count[1] int32, err_word[1] int32)."""
+                 workspace_buf=None, err_word=None, stream=None, z_loss: float = 0.0,
+                 row_loss=None, skip_ignored_blocks: bool = False):
+    """Returns (loss[1] fp32, lse[N] fp32, valid_count[1] int32, err_word[1] int32).
+    With z_loss, row_loss or skip_ignored_blocks set it calls flce_forward_ex."""
+    if z_loss or row_loss is not None or skip_ignored_blocks:
+        return flce_forward_ex(X, W, labels, make_options(ignore_index, smoothing, reduction,
+                                                          z_loss, row_loss, skip_ignored_blocks),
+                               loss=loss, lse=lse, valid_count=valid_count,
+                               workspace_buf=workspace_buf, err_word=err_word, stream=stream)
     N, H, V = _check_inputs(X, W, labels)
     dev = X.device
     dt = _dtype_code(X)
@@ -208,11 +248,36 @@ def flce_forward(X, W, labels, ignore_index: int = -100, smoothing: float = 0.0,
     return loss, lse, valid_count, err_word
 
 
+def flce_forward_ex(X, W, labels, options: FlceOptions, *, loss=None, lse=None,
+                    valid_count=None, workspace_buf=None, err_word=None, stream=None):
+    N, H, V = _check_inputs(X, W, labels)
+    dev = X.device
+    dt = _dtype_code(X)
+    loss = torch.empty(1, dtype=torch.float32, device=dev) if loss is None else loss
+    lse = torch.empty(N, dtype=torch.float32, device=dev) if lse is None else lse
+    valid_count = torch.empty(1, dtype=torch.int32, device=dev) if valid_count is None else valid_count
+    ws = workspace(N, H, V, dt, MODE_FWD, dev) if workspace_buf is None else workspace_buf
+    err_word = new_err_word(dev) if err_word is None else err_word
+    st = lib().flce_forward_ex(_ptr(X), _ptr(W), _ptr(labels), N, H, V, dt, ctypes.byref(options),
+                               _ptr(loss), _ptr(lse), _ptr(valid_count), _ptr(ws), ws.numel(),
+                               _ptr(err_word), _stream(stream))
+    _check(st, "flce_forward_ex")
+    return loss, lse, valid_count, err_word
+
+
 def flce_backward(X, W, labels, lse, valid_count, ignore_index: int = -100,
                   smoothing: float = 0.0, reduction: str = "mean", *, grad_loss=None,
                   dX=None, dW=None, accumulate_dW: bool = False, workspace_buf=None,
-                  err_word=None, stream=None):
-    """Returns (dX [N, H] in X's dtype, dW [V, H] fp32, err_word)."""
+                  err_word=None, stream=None, z_loss: float = 0.0,
+                  skip_ignored_blocks: bool = False):
+    """Returns (dX [N, H] in X's dtype, dW [V, H] fp32, err_word).
+    With z_loss or skip_ignored_blocks set it calls flce_backward_ex."""
+    if z_loss or skip_ignored_blocks:
+        return flce_backward_ex(X, W, labels, lse, valid_count,
+                                make_options(ignore_index, smoothing, reduction, z_loss,
+                                             skip_ignored_blocks=skip_ignored_blocks),
+                                grad_loss=grad_loss, dX=dX, dW=dW, accumulate_dW=accumulate_dW,
+                                workspace_buf=workspace_buf, err_word=err_word, stream=stream)
     N, H, V = _check_inputs(X, W, labels)
     dev = X.device
     dt = _dtype_code(X)
@@ -231,11 +296,40 @@ def flce_backward(X, W, labels, lse, valid_count, ignore_index: int = -100,
     return dX, dW, err_word
 
 
+def flce_backward_ex(X, W, labels, lse, valid_count, options: FlceOptions, *, grad_loss=None,
+                     dX=None, dW=None, accumulate_dW: bool = False, workspace_buf=None,
+                     err_word=None, stream=None):
+    N, H, V = _check_inputs(X, W, labels)
+    dev = X.device
+    dt = _dtype_code(X)
+    dX = torch.empty_like(X) if dX is None else dX
+    if dW is None:
+        if accumulate_dW:
+            raise ValueError("accumulate_dW needs an existing dW")
+        dW = torch.empty(V, H, dtype=torch.float32, device=dev)
+    ws = workspace(N, H, V, dt, MODE_BWD, dev) if workspace_buf is None else workspace_buf
+    err_word = new_err_word(dev) if err_word is None else err_word
+    st = lib().flce_backward_ex(_ptr(X), _ptr(W), _ptr(labels), N, H, V, dt,
+                                ctypes.byref(options), _ptr(lse), _ptr(valid_count),
+                                _ptr(grad_loss), _ptr(dX), _ptr(dW), int(bool(accumulate_dW)),
+                                _ptr(ws), ws.numel(), _ptr(err_word), _stream(stream))
+    _check(st, "flce_backward_ex")
+    return dX, dW, err_word
+
+
 def flce_fwd_bwd(X, W, labels, ignore_index: int = -100, smoothing: float = 0.0,
                  reduction: str = "mean", *, grad_loss=None, loss=None, lse=None,
                  valid_count=None, dX=None, dW=None, accumulate_dW: bool = False,
-                 workspace_buf=None, err_word=None, stream=None):
-    """Returns (loss, lse, valid_count, dX, dW, err_word)."""
+                 workspace_buf=None, err_word=None, stream=None, z_loss: float = 0.0,
+                 row_loss=None, skip_ignored_blocks: bool = False):
+    """Returns (loss, lse, valid_count, dX, dW, err_word).
+    With z_loss, row_loss or skip_ignored_blocks set it calls flce_fwd_bwd_ex."""
+    if z_loss or row_loss is not None or skip_ignored_blocks:
+        return flce_fwd_bwd_ex(X, W, labels, make_options(ignore_index, smoothing, reduction,
+                                                          z_loss, row_loss, skip_ignored_blocks),
+                               grad_loss=grad_loss, loss=loss, lse=lse, valid_count=valid_count,
+                               dX=dX, dW=dW, accumulate_dW=accumulate_dW,
+                               workspace_buf=workspace_buf, err_word=err_word, stream=stream)
     N, H, V = _check_inputs(X, W, labels)
     dev = X.device
     dt = _dtype_code(X)
@@ -254,6 +348,30 @@ def flce_fwd_bwd(X, W, labels, ignore_index: int = -100, smoothing: float = 0.0,
                             _ptr(valid_count), _ptr(dX), _ptr(dW), int(bool(accumulate_dW)),
                             _ptr(ws), ws.numel(), _ptr(err_word), _stream(stream))
     _check(st, "flce_fwd_bwd")
+    return loss, lse, valid_count, dX, dW, err_word
+
+
+def flce_fwd_bwd_ex(X, W, labels, options: FlceOptions, *, grad_loss=None, loss=None, lse=None,
+                    valid_count=None, dX=None, dW=None, accumulate_dW: bool = False,
+                    workspace_buf=None, err_word=None, stream=None):
+    N, H, V = _check_inputs(X, W, labels)
+    dev = X.device
+    dt = _dtype_code(X)
+    loss = torch.empty(1, dtype=torch.float32, device=dev) if loss is None else loss
+    lse = torch.empty(N, dtype=torch.float32, device=dev) if lse is None else lse
+    valid_count = torch.empty(1, dtype=torch.int32, device=dev) if valid_count is None else valid_count
+    dX = torch.empty_like(X) if dX is None else dX
+    if dW is None:
+        if accumulate_dW:
+            raise ValueError("accumulate_dW needs an existing dW")
+        dW = torch.empty(V, H, dtype=torch.float32, device=dev)
+    ws = workspace(N, H, V, dt, MODE_FWD_BWD, dev) if workspace_buf is None else workspace_buf
+    err_word = new_err_word(dev) if err_word is None else err_word
+    st = lib().flce_fwd_bwd_ex(_ptr(X), _ptr(W), _ptr(labels), N, H, V, dt, ctypes.byref(options),
+                               _ptr(grad_loss), _ptr(loss), _ptr(lse), _ptr(valid_count),
+                               _ptr(dX), _ptr(dW), int(bool(accumulate_dW)), _ptr(ws),
+                               ws.numel(), _ptr(err_word), _stream(stream))
+    _check(st, "flce_fwd_bwd_ex")
     return loss, lse, valid_count, dX, dW, err_word
 
 
@@ -311,26 +429,28 @@ def flce_profile_read() -> dict:
 
 class _LinearCrossEntropy(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, X, W, labels, ignore_index, smoothing, reduction):
-        loss, lse, nv, err = flce_forward(X, W, labels, ignore_index, smoothing, reduction)
+    def forward(ctx, X, W, labels, ignore_index, smoothing, reduction, z_loss):
+        loss, lse, nv, err = flce_forward(X, W, labels, ignore_index, smoothing, reduction,
+                                          z_loss=z_loss)
         ctx.save_for_backward(X, W, labels, lse, nv, err)
-        ctx.cfg = (ignore_index, smoothing, reduction)
+        ctx.cfg = (ignore_index, smoothing, reduction, z_loss)
         return loss[0]
 
     @staticmethod
     def backward(ctx, g):
         X, W, labels, lse, nv, err = ctx.saved_tensors
-        ii, eps, red = ctx.cfg
+        ii, eps, red, zl = ctx.cfg
         g1 = g.reshape(1).to(torch.float32).contiguous()
-        dX, dW, _ = flce_backward(X, W, labels, lse, nv, ii, eps, red, grad_loss=g1, err_word=err)
-        return dX, dW.to(W.dtype), None, None, None, None
+        dX, dW, _ = flce_backward(X, W, labels, lse, nv, ii, eps, red, grad_loss=g1, err_word=err,
+                                  z_loss=zl)
+        return dX, dW.to(W.dtype), None, None, None, None, None
 
 
 def linear_cross_entropy(h, W, labels, ignore_index: int = -100, smoothing: float = 0.0,
-                         reduction: str = "mean"):
+                         reduction: str = "mean", z_loss: float = 0.0):
     """Autograd entry with the pages' call shape: linear_cross_entropy(h, W, labels,
     ignore_index=-100).  h may be [..., H]; labels [...] of the same leading shape."""
     H = h.shape[-1]
     return _LinearCrossEntropy.apply(h.reshape(-1, H).contiguous(), W.contiguous(),
                                      labels.reshape(-1).contiguous(), ignore_index, smoothing,
-                                     reduction)
+                                     reduction, z_loss)

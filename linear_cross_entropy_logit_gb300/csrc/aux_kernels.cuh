@@ -15,21 +15,28 @@ constexpr float LN2 = 0.6931471805599453f;
 // (max*log2e, rescaled exp-sum, target logit, logit sum) into
 //   lse_i = m_i + log d_i       ("Chunked and Fused Cross-Entropy ...",
 //                                 "Mathematical Mechanics ...", step 2)
-//   l_i   = valid_i * (lse_i - (1-eps) z_{i,y_i} - (eps/V) sum_j z_ij)
-// and reduces l_i and valid_i over the block in a fixed tree order.
+//   l_i   = valid_i * (lse_i - (1-eps) z_{i,y_i} - (eps/V) sum_j z_ij
+//                    + alpha lse_i^2)            (z-loss term when alpha > 0)
+// writes l_i per row when asked, and reduces l_i and valid_i over the block in
+// a fixed tree order.
 // A label outside [0, V) that is not ignore_index sets FLCE_ERR_LABEL and
 // the row counts as ignored.
 static __global__ void __launch_bounds__(MERGE_THREADS)
     lse_merge_kernel(const float4* __restrict__ partials, int n_groups, int m_pad, int N, int V,
                      const int64_t* __restrict__ labels, long long ignore_index, float smoothing,
-                     float* __restrict__ lse_out, double* __restrict__ block_loss,
-                     int* __restrict__ block_valid, int* err_word) {
+                     float z_loss, float* __restrict__ lse_out, float* __restrict__ row_loss,
+                     double* __restrict__ block_loss, int* __restrict__ block_valid,
+                     int* err_word, const int* __restrict__ block_active, int block_rows) {
   __shared__ double s_loss[MERGE_THREADS];
   __shared__ int s_valid[MERGE_THREADS];
   const int row = blockIdx.x * MERGE_THREADS + threadIdx.x;
   double loss = 0.0;
   int valid = 0;
-  if (row < N) {
+  if (row < N && block_active && !block_active[row / block_rows]) {
+    // a skipped block: every label in it is ignore_index, its logits were not formed
+    lse_out[row] = __int_as_float(0x7fc00000);
+    if (row_loss) row_loss[row] = 0.f;
+  } else if (row < N) {
     float M = -INFINITY;
     for (int g = 0; g < n_groups; ++g) M = fmaxf(M, partials[(size_t)g * m_pad + row].x);
     float S = 0.f, zy = 0.f, zs = 0.f;
@@ -49,9 +56,11 @@ static __global__ void __launch_bounds__(MERGE_THREADS)
         valid = 1;
         double l = (double)lse - (1.0 - (double)smoothing) * (double)zy;
         if (smoothing != 0.f) l -= (double)smoothing / (double)V * (double)zs;
+        if (z_loss != 0.f) l += (double)z_loss * (double)lse * (double)lse;
         loss = l;
       }
     }
+    if (row_loss) row_loss[row] = (float)loss;
   }
   s_loss[threadIdx.x] = loss;
   s_valid[threadIdx.x] = valid;
@@ -132,6 +141,49 @@ static __global__ void cast_f32_bf16_kernel(const float4* __restrict__ in, uint2
        i += (size_t)gridDim.x * blockDim.x) {
     const float4 v = in[i];
     out[i] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+  }
+}
+
+// Token blocks of `block_rows` rows that hold at least one label other than
+// ignore_index: per-block flag, and the ascending list of active blocks with
+// its length (a single block of threads; the scan runs in block order).
+static __global__ void __launch_bounds__(MERGE_THREADS)
+    active_blocks_kernel(const int64_t* __restrict__ labels, int N, long long ignore_index,
+                         int block_rows, int n_blocks, int* __restrict__ flags,
+                         int* __restrict__ list, int* __restrict__ count) {
+  __shared__ int s_base;
+  __shared__ int s_flag[MERGE_THREADS];
+  if (threadIdx.x == 0) s_base = 0;
+  __syncthreads();
+  for (int b0 = 0; b0 < n_blocks; b0 += MERGE_THREADS) {
+    const int b = b0 + threadIdx.x;
+    int active = 0;
+    if (b < n_blocks) {
+      const int r1 = min(N, (b + 1) * block_rows);
+      for (int r = b * block_rows; r < r1 && !active; ++r) active = labels[r] != ignore_index;
+      flags[b] = active;
+    }
+    s_flag[threadIdx.x] = active;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int base = s_base;
+      for (int t = 0; t < MERGE_THREADS && b0 + t < n_blocks; ++t)
+        if (s_flag[t]) list[base++] = b0 + t;
+      s_base = base;
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *count = s_base;
+}
+
+// dX_acc rows of skipped blocks are zero (their dZ rows are).
+static __global__ void zero_skipped_rows_kernel(const int* __restrict__ flags, int block_rows,
+                                                float* __restrict__ acc, int N, int H) {
+  const size_t total = (size_t)N * H;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const int row = (int)(i / H);
+    if (!flags[row / block_rows]) acc[i] = 0.f;
   }
 }
 

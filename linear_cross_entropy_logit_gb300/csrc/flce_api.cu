@@ -94,8 +94,9 @@ struct Plan {
   int m_blocks, m_pad, v_tiles, group_len, n_groups, merge_blocks;
   int64_t chunk;
   int n_chunks;
-  size_t off_scalars, off_partials, off_block_loss, off_block_valid, off_dz, off_dxacc,
-      off_xcast, off_wcast, total;
+  size_t off_scalars, off_blocks, off_partials, off_block_loss, off_block_valid, off_dz,
+      off_dxacc, off_xcast, off_wcast, total;
+  int n_blocks128;  // token blocks of 128 rows (the finest skip granularity)
 };
 
 bool shape_ok(int64_t N, int64_t H, int64_t V) {
@@ -142,6 +143,10 @@ bool make_plan(int64_t N, int64_t H, int64_t V, flce_dtype dtype, int mode, Plan
   size_t off = 0;
   p.off_scalars = off;
   off += kAlign;
+  // skip lists: flags[nb], list[nb], count -- nb counted at 128-row granularity
+  p.n_blocks128 = (int)ceil_div(std::max<int64_t>(N, 1), BM);
+  p.off_blocks = off;
+  off = align_up(off + (size_t)(2 * p.n_blocks128 + 1) * sizeof(int), kAlign);
   p.off_partials = p.off_block_loss = p.off_block_valid = 0;
   if (fwd) {
     p.off_partials = off;
@@ -350,6 +355,9 @@ struct Common {
   const int64_t* labels;
   int64_t N, H, V, ignore_index;
   float smoothing;
+  float z_loss;
+  float* row_loss;
+  int skip_ignored;
   flce_dtype dtype;
   flce_reduction reduction;
   void* ws;
@@ -363,6 +371,8 @@ flce_status validate_common(const Common& c, int mode, Plan* pl) {
   if (c.dtype != FLCE_BF16 && c.dtype != FLCE_FP32) return FLCE_ERR_ARG;
   if (c.reduction != FLCE_MEAN && c.reduction != FLCE_SUM) return FLCE_ERR_ARG;
   if (!(c.smoothing >= 0.f && c.smoothing < 1.f)) return FLCE_ERR_ARG;
+  if (!(c.z_loss >= 0.f && c.z_loss < 1e30f)) return FLCE_ERR_ARG;
+  if (c.row_loss && !aligned(c.row_loss, 4)) return FLCE_ERR_ARG;
   if (!c.err_word) return FLCE_ERR_ARG;
   if (c.N > 0) {
     if (!c.X || !c.labels) return FLCE_ERR_ARG;
@@ -373,6 +383,33 @@ flce_status validate_common(const Common& c, int mode, Plan* pl) {
   if (!make_plan(c.N, c.H, c.V, c.dtype, mode, pl)) return FLCE_ERR_ARG;
   if (!c.ws || !aligned(c.ws, kAlign)) return FLCE_ERR_WORKSPACE;
   if (c.ws_bytes < pl->total) return FLCE_ERR_WORKSPACE;
+  return FLCE_OK;
+}
+
+// Skip lists for SFT-style masking: token blocks of `tile_rows(pair)` rows with
+// at least one label other than ignore_index.
+struct SkipLists {
+  const int* flags = nullptr;
+  const int* list = nullptr;
+  const int* count = nullptr;
+  int block_rows = 1;
+};
+
+flce_status build_skip_lists(const Common& c, const Plan& pl, bool pair, SkipLists* out) {
+  *out = SkipLists{};
+  if (!c.skip_ignored || c.N == 0) return FLCE_OK;
+  int* base = reinterpret_cast<int*>(static_cast<uint8_t*>(c.ws) + pl.off_blocks);
+  const int rows = tile_rows(pair);
+  const int nb = (int)ceil_div(c.N, rows);
+  active_blocks_kernel<<<1, MERGE_THREADS, 0, c.st>>>(c.labels, (int)c.N, c.ignore_index, rows,
+                                                       nb, base, base + pl.n_blocks128,
+                                                       base + 2 * pl.n_blocks128);
+  ++g_launches;
+  FLCE_CUDA(cudaGetLastError());
+  out->flags = base;
+  out->list = base + pl.n_blocks128;
+  out->count = base + 2 * pl.n_blocks128;
+  out->block_rows = rows;
   return FLCE_OK;
 }
 
@@ -409,6 +446,8 @@ flce_status run_forward(const Common& c, const Plan& pl, int dev, int sms, const
   int* block_valid = reinterpret_cast<int*>(ws + pl.off_block_valid);
   if (c.N > 0) {
     const bool pair = use_pair();
+    SkipLists sk;
+    FLCE_TRY(build_skip_lists(c, pl, pair, &sk));
     CUtensorMap tmX, tmW;
     FLCE_TRY(map_kmajor(&tmX, Xb, c.H, c.N, c.H, BM));
     FLCE_TRY(map_kmajor(&tmW, Wb, c.H, c.V, c.H, b_box_rows(pair)));
@@ -432,12 +471,15 @@ flce_status run_forward(const Common& c, const Plan& pl, int dev, int sms, const
     p.m_pad = pl.m_pad;
     p.l2_keep_b = 0;
     p.l2_keep_frac = l2_keep_fraction((double)c.N * c.H * 2);
+    p.row_list = sk.list;
+    p.row_count = sk.count;
     p.err_word = c.err_word;
     p.timeout_ns = kTimeoutNs;
     FLCE_TRY((launch_tile<Epi::kLse, false, false>(pair, dev, sms, tmX, tmW, tmX, p, c.st, 0)));
     lse_merge_kernel<<<pl.merge_blocks, MERGE_THREADS, 0, c.st>>>(
         p.partials, pl.n_groups, pl.m_pad, (int)c.N, (int)c.V, c.labels, c.ignore_index,
-        c.smoothing, lse, block_loss, block_valid, c.err_word);
+        c.smoothing, c.z_loss, lse, c.row_loss, block_loss, block_valid, c.err_word, sk.flags,
+        sk.block_rows);
     ++g_launches;
     FLCE_CUDA(cudaGetLastError());
   }
@@ -474,6 +516,14 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
 
   const bool pair = use_pair();
   const int m_blocks_tok = (int)ceil_div(N, tile_rows(pair));
+  SkipLists sk;
+  FLCE_TRY(build_skip_lists(c, pl, pair, &sk));
+  if (sk.flags) {
+    zero_skipped_rows_kernel<<<2 * sms, 256, 0, c.st>>>(sk.flags, sk.block_rows, dx_acc, (int)N,
+                                                         (int)H);
+    ++g_launches;
+    FLCE_CUDA(cudaGetLastError());
+  }
   const int h_blocks = (int)ceil_div(H, BN);
   for (int ci = 0; ci < pl.n_chunks; ++ci) {
     const int64_t v0 = (int64_t)ci * Cv;
@@ -504,6 +554,9 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
     p3.col_base = (int)v0;
     p3.col_limit = (int)w;
     p3.smoothing = c.smoothing;
+    p3.z_loss = c.z_loss;
+    p3.row_list = sk.list;
+    p3.row_count = sk.count;
     p3.lse = lse;
     p3.scale = scale;
     p3.l2_keep_b = 0;  // X is reused by every wave; the W tile is shared within one
@@ -524,6 +577,9 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
     p4.num_units = p4.m_blocks * h_blocks;
     p4.m_fastest = 0;
     p4.reduce_add = accumulate ? 1 : 0;
+    p4.k_list = sk.list;
+    p4.k_count = sk.count;
+    p4.k_per_entry = tile_rows(pair) / BK;
     p4.l2_keep_b = 1;  // X again; the dZ column block is shared within one wave
     p4.l2_keep_frac = l2_keep_fraction((double)N * H * 2);
     p4.err_word = c.err_word;
@@ -542,6 +598,8 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
     p5.num_units = m_blocks_tok * h_blocks;
     p5.m_fastest = 0;
     p5.reduce_add = ci > 0 ? 1 : 0;
+    p5.row_list = sk.list;
+    p5.row_count = sk.count;
     p5.l2_keep_b = 1;  // the W chunk; the dZ row block is shared within one wave
     p5.l2_keep_frac = l2_keep_fraction((double)w * H * 2);
     p5.err_word = c.err_word;
@@ -566,7 +624,7 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
 // ===========================================================================
 extern "C" {
 
-int flce_abi_version(void) { return 101; }
+int flce_abi_version(void) { return 102; }
 
 const char* flce_status_string(flce_status s) {
   switch (s) {
@@ -648,14 +706,67 @@ size_t flce_workspace_size(int64_t N, int64_t H, int64_t V, flce_dtype dtype, in
   return pl.total;
 }
 
-flce_status flce_forward(const void* X, const void* W, const int64_t* labels, int64_t N,
-                         int64_t H, int64_t V, int64_t ignore_index, float smoothing,
-                         flce_dtype dtype, flce_reduction reduction, float* loss, float* lse,
-                         int32_t* valid_count, void* workspace, size_t ws_bytes,
-                         int32_t* err_word, void* stream) {
+void flce_options_init(flce_options* opt) {
+  if (!opt) return;
+  opt->struct_size = sizeof(flce_options);
+  opt->ignore_index = -100;
+  opt->smoothing = 0.f;
+  opt->z_loss = 0.f;
+  opt->reduction = FLCE_MEAN;
+  opt->row_loss = nullptr;
+  opt->skip_ignored_blocks = 0;
+}
+
+}  // extern "C"
+
+namespace {
+
+bool options_ok(const flce_options* opt) {
+  return opt && opt->struct_size == sizeof(flce_options);
+}
+
+Common make_common(const void* X, const void* W, const int64_t* labels, int64_t N, int64_t H,
+                   int64_t V, flce_dtype dtype, const flce_options* o, void* ws, size_t ws_bytes,
+                   int32_t* err_word, void* stream) {
+  return Common{X,
+                W,
+                labels,
+                N,
+                H,
+                V,
+                o->ignore_index,
+                o->smoothing,
+                o->z_loss,
+                o->row_loss,
+                o->skip_ignored_blocks,
+                dtype,
+                o->reduction,
+                ws,
+                ws_bytes,
+                err_word,
+                static_cast<cudaStream_t>(stream)};
+}
+
+flce_options defaults(int64_t ignore_index, float smoothing, flce_reduction reduction) {
+  flce_options o;
+  flce_options_init(&o);
+  o.ignore_index = ignore_index;
+  o.smoothing = smoothing;
+  o.reduction = reduction;
+  return o;
+}
+
+}  // namespace
+
+extern "C" {
+
+flce_status flce_forward_ex(const void* X, const void* W, const int64_t* labels, int64_t N,
+                            int64_t H, int64_t V, flce_dtype dtype, const flce_options* opt,
+                            float* loss, float* lse, int32_t* valid_count, void* workspace,
+                            size_t ws_bytes, int32_t* err_word, void* stream) {
   g_launches = 0;
-  Common c{X, W, labels, N, H, V, ignore_index, smoothing, dtype, reduction,
-           workspace, ws_bytes, err_word, static_cast<cudaStream_t>(stream)};
+  if (!options_ok(opt)) return FLCE_ERR_ARG;
+  Common c = make_common(X, W, labels, N, H, V, dtype, opt, workspace, ws_bytes, err_word, stream);
   Plan pl;
   FLCE_TRY(validate_common(c, FLCE_MODE_FWD, &pl));
   if (!loss || !valid_count || (N > 0 && !lse)) return FLCE_ERR_ARG;
@@ -666,15 +777,14 @@ flce_status flce_forward(const void* X, const void* W, const int64_t* labels, in
   return run_forward(c, pl, dev, sms, Xb, Wb, loss, lse, valid_count);
 }
 
-flce_status flce_backward(const void* X, const void* W, const int64_t* labels, int64_t N,
-                          int64_t H, int64_t V, int64_t ignore_index, float smoothing,
-                          flce_dtype dtype, flce_reduction reduction, const float* lse,
-                          const int32_t* valid_count, const float* grad_loss, void* dX,
-                          float* dW, int accumulate_dW, void* workspace, size_t ws_bytes,
-                          int32_t* err_word, void* stream) {
+flce_status flce_backward_ex(const void* X, const void* W, const int64_t* labels, int64_t N,
+                             int64_t H, int64_t V, flce_dtype dtype, const flce_options* opt,
+                             const float* lse, const int32_t* valid_count,
+                             const float* grad_loss, void* dX, float* dW, int accumulate_dW,
+                             void* workspace, size_t ws_bytes, int32_t* err_word, void* stream) {
   g_launches = 0;
-  Common c{X, W, labels, N, H, V, ignore_index, smoothing, dtype, reduction,
-           workspace, ws_bytes, err_word, static_cast<cudaStream_t>(stream)};
+  if (!options_ok(opt)) return FLCE_ERR_ARG;
+  Common c = make_common(X, W, labels, N, H, V, dtype, opt, workspace, ws_bytes, err_word, stream);
   Plan pl;
   FLCE_TRY(validate_common(c, FLCE_MODE_BWD, &pl));
   if (!valid_count || !dW || !aligned(dW, 16)) return FLCE_ERR_ARG;
@@ -687,15 +797,14 @@ flce_status flce_backward(const void* X, const void* W, const int64_t* labels, i
                       accumulate_dW);
 }
 
-flce_status flce_fwd_bwd(const void* X, const void* W, const int64_t* labels, int64_t N,
-                         int64_t H, int64_t V, int64_t ignore_index, float smoothing,
-                         flce_dtype dtype, flce_reduction reduction, const float* grad_loss,
-                         float* loss, float* lse, int32_t* valid_count, void* dX, float* dW,
-                         int accumulate_dW, void* workspace, size_t ws_bytes, int32_t* err_word,
-                         void* stream) {
+flce_status flce_fwd_bwd_ex(const void* X, const void* W, const int64_t* labels, int64_t N,
+                            int64_t H, int64_t V, flce_dtype dtype, const flce_options* opt,
+                            const float* grad_loss, float* loss, float* lse,
+                            int32_t* valid_count, void* dX, float* dW, int accumulate_dW,
+                            void* workspace, size_t ws_bytes, int32_t* err_word, void* stream) {
   g_launches = 0;
-  Common c{X, W, labels, N, H, V, ignore_index, smoothing, dtype, reduction,
-           workspace, ws_bytes, err_word, static_cast<cudaStream_t>(stream)};
+  if (!options_ok(opt)) return FLCE_ERR_ARG;
+  Common c = make_common(X, W, labels, N, H, V, dtype, opt, workspace, ws_bytes, err_word, stream);
   Plan pl;
   FLCE_TRY(validate_common(c, FLCE_MODE_FWD_BWD, &pl));
   if (!loss || !valid_count || !dW || !aligned(dW, 16)) return FLCE_ERR_ARG;
@@ -707,6 +816,38 @@ flce_status flce_fwd_bwd(const void* X, const void* W, const int64_t* labels, in
   FLCE_TRY(run_forward(c, pl, dev, sms, Xb, Wb, loss, lse, valid_count));
   return run_backward(c, pl, dev, sms, Xb, Wb, lse, valid_count, grad_loss, dX, dW,
                       accumulate_dW);
+}
+
+flce_status flce_forward(const void* X, const void* W, const int64_t* labels, int64_t N,
+                         int64_t H, int64_t V, int64_t ignore_index, float smoothing,
+                         flce_dtype dtype, flce_reduction reduction, float* loss, float* lse,
+                         int32_t* valid_count, void* workspace, size_t ws_bytes,
+                         int32_t* err_word, void* stream) {
+  const flce_options o = defaults(ignore_index, smoothing, reduction);
+  return flce_forward_ex(X, W, labels, N, H, V, dtype, &o, loss, lse, valid_count, workspace,
+                         ws_bytes, err_word, stream);
+}
+
+flce_status flce_backward(const void* X, const void* W, const int64_t* labels, int64_t N,
+                          int64_t H, int64_t V, int64_t ignore_index, float smoothing,
+                          flce_dtype dtype, flce_reduction reduction, const float* lse,
+                          const int32_t* valid_count, const float* grad_loss, void* dX,
+                          float* dW, int accumulate_dW, void* workspace, size_t ws_bytes,
+                          int32_t* err_word, void* stream) {
+  const flce_options o = defaults(ignore_index, smoothing, reduction);
+  return flce_backward_ex(X, W, labels, N, H, V, dtype, &o, lse, valid_count, grad_loss, dX, dW,
+                          accumulate_dW, workspace, ws_bytes, err_word, stream);
+}
+
+flce_status flce_fwd_bwd(const void* X, const void* W, const int64_t* labels, int64_t N,
+                         int64_t H, int64_t V, int64_t ignore_index, float smoothing,
+                         flce_dtype dtype, flce_reduction reduction, const float* grad_loss,
+                         float* loss, float* lse, int32_t* valid_count, void* dX, float* dW,
+                         int accumulate_dW, void* workspace, size_t ws_bytes, int32_t* err_word,
+                         void* stream) {
+  const flce_options o = defaults(ignore_index, smoothing, reduction);
+  return flce_fwd_bwd_ex(X, W, labels, N, H, V, dtype, &o, grad_loss, loss, lse, valid_count, dX,
+                         dW, accumulate_dW, workspace, ws_bytes, err_word, stream);
 }
 
 flce_status flce_debug_gemm(const void* A, const void* B, float* D, int64_t M, int64_t Nn,

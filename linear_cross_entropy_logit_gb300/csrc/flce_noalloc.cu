@@ -222,8 +222,8 @@ extern "C" flce_status flce_forward_noalloc(const void* X, const void* W, const 
         <<<grid, NUM_THREADS, gemm_smem_bytes<Epi::kLse, kNaStages, false>(), st>>>(tmX, tmW, tmX, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return na_cuda_fail(e, "forward GEMM launch");
     lse_merge_kernel<<<pl.merge_blocks, MERGE_THREADS, 0, st>>>(
-        p.partials, pl.n_groups, pl.m_pad, (int)N, (int)V, labels, ignore_index, smoothing, lse,
-        block_loss, block_valid, err_word);
+        p.partials, pl.n_groups, pl.m_pad, (int)N, (int)V, labels, ignore_index, smoothing, 0.f,
+        lse, nullptr, block_loss, block_valid, err_word, nullptr, 1);
     if ((e = cudaGetLastError()) != cudaSuccess) return na_cuda_fail(e, "merge launch");
   }
   loss_finalize_kernel<<<1, MERGE_THREADS, 0, st>>>(block_loss, block_valid,

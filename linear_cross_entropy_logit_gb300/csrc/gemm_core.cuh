@@ -90,12 +90,23 @@ struct GemmParams {
   int col_base;           // vocabulary index of D column 0
   int col_limit;          // D columns >= col_limit do not exist
   float smoothing;        // eps
+  float z_loss;           // kDz: z-loss weight alpha (softmax term scaled by 1 + 2 alpha lse)
   float4* partials;       // kLse: [n_groups][m_pad] of (max*log2e, sum, z_y, sum_z)
   int m_pad;              // m_blocks * TILE_M
   const float* lse;       // kDz: per-row log-sum-exp
   const float* scale;     // kDz: device scalar c = grad / N_valid
   // kStore
   int reduce_add;         // 1: TMA reduce-add onto the output, 0: overwrite
+  // Skipping fully ignored token blocks (SFT-style masking).  When row_list is
+  // set, units walk only the row blocks it lists (device count *row_count, in
+  // units of TILE_M rows).  When k_list is set, the contraction walks only the
+  // token blocks it lists (*k_count entries of k_per_entry k-blocks each); a
+  // tile with no active k-block is written as zeros.
+  const int* row_list;
+  const int* row_count;
+  const int* k_list;
+  const int* k_count;
+  int k_per_entry;
   // L2 residency: the operand reused across waves of tiles (0 = A, 1 = B) is
   // loaded with an evict_last policy covering `l2_keep_frac` of its lines.
   int l2_keep_b;
@@ -111,17 +122,41 @@ constexpr int gemm_smem_bytes() {
          1024;
 }
 
-__device__ __forceinline__ void unit_coords(const GemmParams& p, int u, int& mb, int& nb0,
-                                            int& nb1, int& g) {
+// Row-block count and unit count of this launch (after skipping, if any).
+struct UnitSpace {
+  int m_blocks;
+  int num_units;
+};
+
+__device__ __forceinline__ UnitSpace unit_space(const GemmParams& p) {
+  if (p.row_list) {
+    const int cnt = *p.row_count;
+    return {cnt, cnt * p.n_groups};
+  }
+  return {p.m_blocks, p.num_units};
+}
+
+__device__ __forceinline__ void unit_coords(const GemmParams& p, const UnitSpace& us, int u,
+                                            int& mb, int& nb0, int& nb1, int& g) {
   if (p.m_fastest) {
-    mb = u % p.m_blocks;
-    g = u / p.m_blocks;
+    mb = u % us.m_blocks;
+    g = u / us.m_blocks;
   } else {
     g = u % p.n_groups;
     mb = u / p.n_groups;
   }
+  if (p.row_list) mb = p.row_list[mb];
   nb0 = g * p.group_len;
   nb1 = min(nb0 + p.group_len, p.n_blocks);
+}
+
+// Number of k-blocks the contraction walks, and the i-th of them.
+__device__ __forceinline__ int kblock_count(const GemmParams& p, int num_kb) {
+  return p.k_list ? (*p.k_count) * p.k_per_entry : num_kb;
+}
+
+__device__ __forceinline__ int kblock_at(const GemmParams& p, int i) {
+  return p.k_list ? p.k_list[i / p.k_per_entry] * p.k_per_entry + i % p.k_per_entry : i;
 }
 
 // tcgen05.wait::ld with the loaded registers as operands, so no use of them
@@ -218,7 +253,9 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const WaitCtx ctx{abort_flag, p.err_word, p.timeout_ns};
-  const int num_kb = (p.k_size + BK - 1) / BK;
+  const int num_kb_all = (p.k_size + BK - 1) / BK;
+  const int num_kb = kblock_count(p, num_kb_all);
+  const UnitSpace us = unit_space(p);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -228,13 +265,14 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
       const uint64_t keep = l2_policy_evict_last(p.l2_keep_frac);
       const bool keep_a = p.l2_keep_frac > 0.f && !p.l2_keep_b;
       const bool keep_b = p.l2_keep_frac > 0.f && p.l2_keep_b;
-      for (int u = pair_id; u < p.num_units && ok; u += num_pairs) {
+      for (int u = pair_id; u < us.num_units && ok; u += num_pairs) {
         int mb, nb0, nb1, g;
-        unit_coords(p, u, mb, nb0, nb1, g);
+        unit_coords(p, us, u, mb, nb0, nb1, g);
         const int a_row = mb * Cfg::TILE_M + (int)rank * BM;
         for (int nb = nb0; nb < nb1 && ok; ++nb) {
           const int b_row = nb * BN + (int)rank * Cfg::B_ROWS;
-          for (int kb = 0; kb < num_kb; ++kb) {
+          for (int ki = 0; ki < num_kb; ++ki) {
+            const int kb = kblock_at(p, ki);
             const int s = it % STAGES;
             const uint32_t r = it / STAGES;
             if (!mbar_wait(&empty[s], (r & 1u) ^ 1u, ctx)) {
@@ -311,9 +349,9 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
       constexpr uint32_t kMnLbo = MN_BOX_BYTES;
       uint32_t it = 0, tile = 0;
       bool ok = true;
-      for (int u = pair_id; u < p.num_units && ok; u += num_pairs) {
+      for (int u = pair_id; u < us.num_units && ok; u += num_pairs) {
         int mb, nb0, nb1, g;
-        unit_coords(p, u, mb, nb0, nb1, g);
+        unit_coords(p, us, u, mb, nb0, nb1, g);
         for (int nb = nb0; nb < nb1 && ok; ++nb) {
           const uint32_t acc = tile & 1u;
           const uint32_t ra = tile >> 1;
@@ -323,7 +361,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + acc * BN;
-          for (int kb = 0; kb < num_kb; ++kb) {
+          for (int ki = 0; ki < num_kb; ++ki) {
             const int s = it % STAGES;
             const uint32_t r = it / STAGES;
             if (!mbar_wait(&full[s], r & 1u, ctx)) {
@@ -340,9 +378,9 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
               const uint64_t bd = B_MN ? smem_desc_sw128(b_addr + kk * 2048, kMnLbo, 1024)
                                        : smem_desc_sw128(b_addr + kk * 32, 16, 1024);
               if constexpr (PAIR)
-                mma_issue_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+                mma_issue_pair(d_tmem, ad, bd, idesc, (ki | kk) != 0 ? 1u : 0u);
               else
-                mma_issue<false>(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+                mma_issue<false>(d_tmem, ad, bd, idesc, (ki | kk) != 0 ? 1u : 0u);
             }
             if constexpr (PAIR)
               mma_commit_pair_multicast(&empty[s], 0x3);
@@ -376,9 +414,9 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
     float c_scale = 0.f;
     if constexpr (EPI == Epi::kDz) c_scale = *p.scale;
 
-    for (int u = pair_id; u < p.num_units && ok; u += num_pairs) {
+    for (int u = pair_id; u < us.num_units && ok; u += num_pairs) {
       int mb, nb0, nb1, g;
-      unit_coords(p, u, mb, nb0, nb1, g);
+      unit_coords(p, us, u, mb, nb0, nb1, g);
       const int row = mb * Cfg::TILE_M + row_in_tile;
       const int store_row0 = mb * Cfg::TILE_M + (int)rank * BM + q * 32;
       const bool row_ok = row < p.m_size;
@@ -391,10 +429,11 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
       const bool valid = row_ok && label != p.ignore_index;
       const long long lab_rel = label - p.col_base;
 
-      float dz_coef = 0.f, dz_neg_lse2 = 0.f, dz_eps = 0.f, dz_tgt = 0.f;
+      float dz_coef = 0.f, dz_pcoef = 0.f, dz_neg_lse2 = 0.f, dz_eps = 0.f, dz_tgt = 0.f;
       if constexpr (EPI == Epi::kDz) {
         const float lse_r = row_ok ? p.lse[row] : 0.f;
         dz_coef = valid ? c_scale : 0.f;
+        dz_pcoef = dz_coef * fmaf(2.f * p.z_loss, lse_r, 1.f);
         dz_neg_lse2 = -lse_r * LOG2E;
         dz_eps = dz_coef * p.smoothing / (float)p.vocab;
         dz_tgt = dz_coef * (1.f - p.smoothing);
@@ -463,8 +502,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
             for (int j = 0; j < 32; ++j) {
               const float za = __uint_as_float(r0[j]);
               const float zb = __uint_as_float(r1[j]);
-              float da = fmaf(dz_coef, ex2_approx(fmaf(za, LOG2E, dz_neg_lse2)), -dz_eps);
-              float db = fmaf(dz_coef, ex2_approx(fmaf(zb, LOG2E, dz_neg_lse2)), -dz_eps);
+              float da = fmaf(dz_pcoef, ex2_approx(fmaf(za, LOG2E, dz_neg_lse2)), -dz_eps);
+              float db = fmaf(dz_pcoef, ex2_approx(fmaf(zb, LOG2E, dz_neg_lse2)), -dz_eps);
               if (off == j) da -= dz_tgt;
               if (off == j + 32) db -= dz_tgt;
               r0[j] = __float_as_uint(da);
@@ -494,6 +533,10 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
             uint32_t r[32];
             tmem_ld_32x32b_x32(taddr + sl * 32, r);
             tmem_ld_wait_regs(r);
+            if (num_kb == 0) {  // every token block skipped: the product is zero
+#pragma unroll
+              for (int j = 0; j < 32; ++j) r[j] = 0u;
+            }
             const uint32_t buf = stag0 + (sl & 1) * STAGING_BUF_BYTES;
             if (lane == 0) bulk_wait_group_read<1>();
             __syncwarp();

@@ -23,6 +23,10 @@ positions, 4 Zipf rank-to-token permutation, 5 scaled W rows):
     seeded permutation of [0, V).
   * ignore positions: the first ``n_ignore`` entries of a seeded permutation
     of [0, N) get the label ``ignore_index``.
+  * instruction-tuning masks (``labels="sft"``): N tokens are sequences of
+    ``seq_len``; sequence b ignores its first floor(u_b * seq_len) tokens (the
+    prompt), u_b uniform in ``prompt_frac``, drawn from stream k = 6; the other
+    labels are uniform.
   * scaled W rows: ``n_scaled`` distinct rows chosen by a seeded permutation,
     multiplied by ``row_scale`` before rounding.
 """
@@ -57,6 +61,8 @@ class WorkloadSpec:
     w_row_scale: float = 1.0
     ignore_index: int = IGNORE_INDEX
     reduction: str = "mean"
+    seq_len: int = 0                       # "sft" labels: tokens per sequence
+    prompt_frac: tuple = (0.2, 0.8)        # "sft" labels: masked prompt share per sequence
 
     @property
     def flops_fwd_bwd(self) -> float:
@@ -77,7 +83,13 @@ GEMMA = WorkloadSpec("gemma2_n32768", N=32768, H=2304, V=256000, dtype="bf16",
                      labels="zipf", n_ignore=int(0.05 * 32768),
                      n_scaled_w_rows=2560, w_row_scale=8.0)
 
-CONFIGS = {s.name: s for s in (TINY, LLAMA, LLAMA_LONG, QWEN, GEMMA)}
+# Instruction tuning on the Llama-3 shape: 4 sequences of 4096 tokens whose
+# prompts (20-80% of each sequence) are masked ("Chunked and Fused
+# Cross-Entropy ...", "Numerical Considerations ...", item 2).
+LLAMA_SFT = WorkloadSpec("llama3_sft_n16384", N=16384, H=4096, V=128256, dtype="bf16",
+                         labels="sft", seq_len=4096)
+
+CONFIGS = {s.name: s for s in (TINY, LLAMA, LLAMA_LONG, QWEN, GEMMA, LLAMA_SFT)}
 
 
 def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
@@ -186,6 +198,14 @@ def make_labels(spec: WorkloadSpec, seed: int, N: Optional[int] = None) -> np.nd
         labels = _rng(seed, 2).integers(0, spec.V, size=N, dtype=np.int64)
     elif spec.labels == "zipf":
         labels = zipf_labels(_rng(seed, 2), _rng(seed, 4), N, spec.V, spec.zipf_s)
+    elif spec.labels == "sft":
+        labels = _rng(seed, 2).integers(0, spec.V, size=N, dtype=np.int64)
+        S = spec.seq_len if spec.seq_len > 0 else N
+        n_seq = (N + S - 1) // S
+        u = _rng(seed, 6).uniform(spec.prompt_frac[0], spec.prompt_frac[1], size=n_seq)
+        for b in range(n_seq):
+            start = b * S
+            labels[start:min(N, start + int(u[b] * S))] = spec.ignore_index
     else:
         raise ValueError(f"unknown label law {spec.labels!r}")
     n_ign = min(spec.n_ignore, N)

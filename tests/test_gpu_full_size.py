@@ -7,7 +7,8 @@ fp64 oracle:
   * dW on sampled vocabulary rows (the most frequent labels, random rows, and
     for the Gemma-shaped workload some of the x8-scaled rows), each computed
     by the oracle one by one from its own lse;
-  * the property sum_j dW_j = 0 on the whole GPU dW, relative to sum_j |dW_j|.
+  * the property sum_j dW_j = 0 (with z-loss: sum_i 2 c alpha lse_i x_i) on
+    the whole GPU dW, relative to sum_j |dW_j|.
 Each case takes from ~20 s (Llama shape) to ~2 min (Gemma shape) of oracle time
 on the host.
 """
@@ -20,11 +21,13 @@ from tests.gpu_util import GRAD_REL_FRO, LOSS_REL, LSE_ABS, rel_err, rel_fro, to
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
-WORKLOADS = ["llama3_n8192", "llama3_long_n16384", "qwen25_n16384", "gemma2_n32768"]
+WORKLOADS = [("llama3_n8192", 0.0), ("llama3_long_n16384", 0.0), ("qwen25_n16384", 0.0),
+             ("gemma2_n32768", 0.0), ("llama3_n8192", 1e-4)]
 
 
-@pytest.mark.parametrize("name", WORKLOADS)
-def test_full_size_parity(name):
+@pytest.mark.parametrize("name,z_loss", WORKLOADS,
+                         ids=[n + (f"-zloss{z:g}" if z else "") for n, z in WORKLOADS])
+def test_full_size_parity(name, z_loss):
     import torch
     from linear_cross_entropy_logit_gb300 import binding as B
 
@@ -34,7 +37,8 @@ def test_full_size_parity(name):
     N, V = spec.N, spec.V
     ii, eps = spec.ignore_index, spec.smoothing
     X, W, y = to_device(wl)
-    loss, lse, nv, dX, dW, err = B.flce_fwd_bwd(X, W, y, ii, eps, spec.reduction)
+    loss, lse, nv, dX, dW, err = B.flce_fwd_bwd(X, W, y, ii, eps, spec.reduction,
+                                                z_loss=z_loss)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     got_lse = lse.double().cpu().numpy()
@@ -51,20 +55,23 @@ def test_full_size_parity(name):
     vrows = np.unique(np.concatenate(vrows))
     got_dx = dX[torch.from_numpy(rows).cuda()].double().cpu().numpy()
     got_dw = dW[torch.from_numpy(vrows).cuda()].double().cpu().numpy()
-    # sum_j dW_j = 0 on the whole GPU output, relative to sum_j |dW_j|
-    col_sum = dW.double().sum(dim=0).norm().item()
+    # sum_j dW_j on the whole GPU output (0, or sum_i 2 c alpha lse_i x_i with
+    # z-loss), relative to sum_j |dW_j|
+    col_sum = dW.double().sum(dim=0).cpu().numpy()
     row_norm_sum = dW.double().norm(dim=1).sum().item()
     del X, W, dX, dW
     torch.cuda.empty_cache()
 
-    f = O.forward(wl.x, wl.w, wl.labels, ii, eps, spec.reduction)
+    f = O.forward(wl.x, wl.w, wl.labels, ii, eps, spec.reduction, z_loss=z_loss)
     assert int(nv.item()) == f.n_valid
     assert rel_err(loss.item(), f.loss) <= LOSS_REL, (loss.item(), f.loss)
     assert np.max(np.abs(got_lse - f.lse)) <= LSE_ABS
     c = O.grad_scale(f.n_valid, spec.reduction)
-    want_dx = O.dx_rows(wl.x, wl.w, wl.labels, rows, c, ii, eps)
+    want_dx = O.dx_rows(wl.x, wl.w, wl.labels, rows, c, ii, eps, z_loss)
     assert rel_fro(got_dx, want_dx) <= GRAD_REL_FRO
     assert np.all(got_dx[np.isin(rows, ignored)] == 0.0)
-    want_dw = O.dw_rows(wl.x, wl.w, wl.labels, vrows, f.lse, c, ii, eps)
+    want_dw = O.dw_rows(wl.x, wl.w, wl.labels, vrows, f.lse, c, ii, eps, z_loss)
     assert rel_fro(got_dw, want_dw) <= GRAD_REL_FRO
-    assert col_sum / row_norm_sum <= 1e-3
+    valid = (wl.labels != ii).astype(np.float64)
+    want_col = 2.0 * c * z_loss * (valid * f.lse) @ O.upcast(wl.x) if z_loss else 0.0
+    assert np.linalg.norm(col_sum - want_col) / row_norm_sum <= 1e-3

@@ -28,30 +28,38 @@ def _auto_chunk():
     B.flce_set_cta_pair(1)
 
 
-def run_fwd_bwd(wl, reduction="mean", grad=None, chunk=0, dW0=None):
+def run_fwd_bwd(wl, reduction="mean", grad=None, chunk=0, dW0=None, z_loss=0.0,
+                row_loss=False, skip=False):
     import torch
     from linear_cross_entropy_logit_gb300 import binding as B
     B.flce_set_vocab_chunk(chunk)
     X, W, y = to_device(wl)
     g = None if grad is None else torch.tensor([grad], dtype=torch.float32, device="cuda")
     dW = None if dW0 is None else torch.from_numpy(dW0.astype(np.float32)).cuda()
+    rl = torch.full((wl.N,), float("nan"), device="cuda") if row_loss else None
     loss, lse, nv, dX, dW, err = B.flce_fwd_bwd(
         X, W, y, wl.spec.ignore_index, wl.spec.smoothing, reduction, grad_loss=g, dW=dW,
-        accumulate_dW=dW0 is not None)
+        accumulate_dW=dW0 is not None, z_loss=z_loss, row_loss=rl, skip_ignored_blocks=skip)
     torch.cuda.synchronize()
-    return dict(loss=float(loss.item()), lse=tensor_f64(lse), nv=int(nv.item()),
-                dX=tensor_f64(dX), dW=tensor_f64(dW), err=int(err.item()))
+    out = dict(loss=float(loss.item()), lse=tensor_f64(lse), nv=int(nv.item()),
+               dX=tensor_f64(dX), dW=tensor_f64(dW), err=int(err.item()))
+    if row_loss:
+        out["row_loss"] = tensor_f64(rl)
+    return out
 
 
-def check_against_oracle(wl, got, reduction="mean", grad=1.0, dW0=None):
-    f = O.forward(wl.x, wl.w, wl.labels, wl.spec.ignore_index, wl.spec.smoothing, reduction)
+def check_against_oracle(wl, got, reduction="mean", grad=1.0, dW0=None, z_loss=0.0,
+                         lse_rows="all"):
+    f = O.forward(wl.x, wl.w, wl.labels, wl.spec.ignore_index, wl.spec.smoothing, reduction,
+                  z_loss=z_loss)
     b = O.backward(wl.x, wl.w, wl.labels, wl.spec.ignore_index, wl.spec.smoothing, reduction,
-                   grad_loss=grad, dW_in=dW0)
+                   grad_loss=grad, dW_in=dW0, z_loss=z_loss)
     assert got["err"] == 0
     assert got["nv"] == f.n_valid
     assert rel_err(got["loss"], f.loss) <= LOSS_REL, (got["loss"], f.loss)
     if wl.N:
-        assert np.max(np.abs(got["lse"] - f.lse)) <= LSE_ABS
+        keep = np.isfinite(got["lse"]) if lse_rows == "finite" else slice(None)
+        assert np.max(np.abs(got["lse"][keep] - f.lse[keep])) <= LSE_ABS
         assert rel_fro(got["dX"], b.dX) <= GRAD_REL_FRO
     assert rel_fro(got["dW"], b.dW) <= GRAD_REL_FRO
     return f, b
@@ -241,3 +249,79 @@ def test_l2_hints_do_not_change_results():
     assert a["loss"] == b["loss"]
     for k in ("lse", "dX", "dW"):
         assert np.array_equal(a[k], b[k])
+
+
+@pytest.mark.parametrize("z_loss", [1e-4, 0.05])
+def test_z_loss(z_loss):
+    """z-loss: each valid token adds alpha * lse^2; the dZ softmax term is
+    scaled by 1 + 2 alpha lse."""
+    wl = I.make_workload(spec(N=400, H=192, V=2500, n_ignore=25, smoothing=0.1, w_std=0.1),
+                         seed=17)
+    got = run_fwd_bwd(wl, z_loss=z_loss)
+    check_against_oracle(wl, got, z_loss=z_loss)
+
+
+def test_z_loss_separate_calls_and_sum():
+    import torch
+    from linear_cross_entropy_logit_gb300 import binding as B
+    wl = I.make_workload(spec(N=300, H=128, V=1800, n_ignore=20), seed=18)
+    X, W, y = to_device(wl)
+    loss, lse, nv, err = B.flce_forward(X, W, y, -100, 0.0, "sum", z_loss=0.01)
+    dX, dW, err2 = B.flce_backward(X, W, y, lse, nv, -100, 0.0, "sum", z_loss=0.01)
+    torch.cuda.synchronize()
+    got = dict(loss=float(loss.item()), lse=tensor_f64(lse), nv=int(nv.item()),
+               dX=tensor_f64(dX), dW=tensor_f64(dW), err=int(err.item()) | int(err2.item()))
+    check_against_oracle(wl, got, reduction="sum", z_loss=0.01)
+
+
+def test_per_token_loss():
+    """reduction 'none': every token's loss, 0 on ignored rows."""
+    wl = I.make_workload(spec(N=333, H=96, V=1200, n_ignore=33, smoothing=0.1), seed=19)
+    got = run_fwd_bwd(wl, row_loss=True, z_loss=0.001)
+    f = O.forward(wl.x, wl.w, wl.labels, -100, 0.1, z_loss=0.001)
+    assert np.max(np.abs(got["row_loss"] - f.row_loss)) <= LSE_ABS
+    assert np.all(got["row_loss"][wl.labels == -100] == 0.0)
+    assert rel_err(got["row_loss"].sum() / f.n_valid, f.loss) <= LOSS_REL
+
+
+@pytest.mark.parametrize("pair", [1, 0], ids=["cta_pair", "single_cta"])
+def test_skip_ignored_blocks_sft(pair):
+    """Whole token blocks whose labels are all ignored are skipped: loss, dX, dW
+    as the oracle's; lse equal on kept rows and NaN on skipped ones."""
+    from linear_cross_entropy_logit_gb300 import binding as B
+    B.flce_set_cta_pair(pair)
+    wl = I.make_workload(spec(N=2048, H=192, V=3000, labels="sft", seq_len=512,
+                              prompt_frac=(0.3, 0.9), smoothing=0.1), seed=20)
+    got = run_fwd_bwd(wl, skip=True, z_loss=1e-3, row_loss=True)
+    f, _ = check_against_oracle(wl, got, z_loss=1e-3, lse_rows="finite")
+    rows = 256 if pair else 128
+    blocks = wl.labels.reshape(-1, rows)
+    skipped = np.all(blocks == -100, axis=1).repeat(rows)
+    assert skipped.any() and not skipped.all()
+    assert np.all(np.isnan(got["lse"][skipped])) and np.all(np.isfinite(got["lse"][~skipped]))
+    assert np.all(got["row_loss"][skipped] == 0.0)
+    full = run_fwd_bwd(wl, z_loss=1e-3)
+    assert rel_err(got["loss"], full["loss"]) <= 1e-6
+    assert rel_fro(got["dX"], full["dX"]) <= 1e-6 and rel_fro(got["dW"], full["dW"]) <= 1e-6
+
+
+def test_skip_ignored_blocks_all_ignored():
+    wl = I.make_workload(spec(N=600, H=64, V=700, n_ignore=600), seed=21)
+    got = run_fwd_bwd(wl, skip=True)
+    assert got["err"] == 0 and got["nv"] == 0 and got["loss"] == 0.0
+    assert np.all(got["dX"] == 0.0) and np.all(got["dW"] == 0.0)
+    assert np.all(np.isnan(got["lse"]))
+
+
+def test_skip_with_separate_calls_and_chunks():
+    import torch
+    from linear_cross_entropy_logit_gb300 import binding as B
+    B.flce_set_vocab_chunk(512)
+    wl = I.make_workload(spec(N=1500, H=136, V=2100, labels="sft", seq_len=500), seed=22)
+    X, W, y = to_device(wl)
+    loss, lse, nv, err = B.flce_forward(X, W, y, skip_ignored_blocks=True)
+    dX, dW, err2 = B.flce_backward(X, W, y, lse, nv, skip_ignored_blocks=True)
+    torch.cuda.synchronize()
+    got = dict(loss=float(loss.item()), lse=tensor_f64(lse), nv=int(nv.item()),
+               dX=tensor_f64(dX), dW=tensor_f64(dW), err=int(err.item()) | int(err2.item()))
+    check_against_oracle(wl, got, lse_rows="finite")

@@ -63,3 +63,15 @@ def test_configs_match_stated_shapes():
     assert (c["llama3_n8192"].N, c["llama3_n8192"].n_ignore) == (8192, 410)
     assert (c["qwen25_n16384"].V, c["qwen25_n16384"].smoothing) == (152064, 0.1)
     assert (c["gemma2_n32768"].n_ignore, c["gemma2_n32768"].n_scaled_w_rows) == (1638, 2560)
+
+
+def test_sft_prompt_spans():
+    spec = I.custom_spec("t", N=1000, H=8, V=50, dtype="fp32", labels="sft", seq_len=250,
+                         prompt_frac=(0.3, 0.6))
+    lab = I.make_labels(spec, 0)
+    for b in range(4):
+        seq = lab[b * 250:(b + 1) * 250]
+        ign = np.flatnonzero(seq == I.IGNORE_INDEX)
+        # a contiguous prefix of 30-60% of the sequence is masked
+        assert len(ign) == ign[-1] + 1 and 75 <= len(ign) <= 150
+        assert np.all(seq[len(ign):] >= 0)

@@ -36,7 +36,7 @@ def test_header_exports_all(L):
 
 
 def test_status_strings_and_version(L):
-    assert L.flce_abi_version() == 101
+    assert L.flce_abi_version() == 102
     for s in range(7):
         assert L.flce_status_string(s).decode().startswith("FLCE_")
 
@@ -116,4 +116,20 @@ def test_argument_errors_without_gpu(L):
     # missing err_word
     st = L.flce_fwd_bwd(P(fake), P(fake), P(fake), 4, 16, 16, -100, 0.0, 0, 0, None, P(fake),
                         P(fake), P(fake), P(fake), P(fake), 0, P(fake), 1 << 20, None, None)
+    assert st == B.FLCE_ERR_ARG
+
+
+def test_options_struct_layout(L):
+    """The ctypes mirror of flce_options has the C struct's size and defaults."""
+    from linear_cross_entropy_logit_gb300 import binding as B
+    o = B.FlceOptions()
+    L.flce_options_init(ctypes.byref(o))
+    assert o.struct_size == ctypes.sizeof(B.FlceOptions)
+    assert (o.ignore_index, o.smoothing, o.z_loss, o.reduction, o.row_loss) == (-100, 0.0, 0.0, 0, None)
+    # a struct of another size is rejected before any CUDA call
+    o.struct_size = 8
+    P = ctypes.c_void_p
+    fake = 1 << 20
+    st = L.flce_forward_ex(P(fake), P(fake), P(fake), 4, 16, 16, 0, ctypes.byref(o), P(fake),
+                           P(fake), P(fake), P(fake), 1 << 20, P(fake), None)
     assert st == B.FLCE_ERR_ARG
