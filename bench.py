@@ -52,6 +52,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--l2-hints", action="store_true",
                     help="evict_last L2 policy for the operand re-read on every wave of tiles")
+    ap.add_argument("--skip-ignored", action="store_true",
+                    help="skip token blocks whose labels are all ignore_index")
     ap.add_argument("--z-loss", type=float, default=0.0,
                     help="z-loss weight alpha (adds alpha * lse^2 per valid token)")
     ap.add_argument("--single-cta", action="store_true",
@@ -250,7 +252,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     def step():
         B.flce_fwd_bwd(X, W, y, spec.ignore_index, spec.smoothing, spec.reduction, loss=loss,
                        lse=lse, valid_count=nv, dX=dX, dW=dW, workspace_buf=ws, err_word=err,
-                       stream=stream, z_loss=args.z_loss)
+                       stream=stream, z_loss=args.z_loss,
+                       skip_ignored_blocks=args.skip_ignored)
         return B.last_launch_count()
 
     for _ in range(max(args.warmup, 0)):
@@ -335,7 +338,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             lo, ls, dx, dw = sl["out"]
             B.flce_fwd_bwd(xd, wd, yd, spec.ignore_index, spec.smoothing, spec.reduction,
                            loss=lo, lse=ls, valid_count=sl["nv"], dX=dx, dW=dw,
-                           workspace_buf=ws, err_word=err, stream=stream, z_loss=args.z_loss)
+                           workspace_buf=ws, err_word=err, stream=stream, z_loss=args.z_loss,
+                           skip_ignored_blocks=args.skip_ignored)
             sl["ev_comp"].record(stream)
             with torch.cuda.stream(s_down):
                 s_down.wait_event(sl["ev_comp"])
@@ -372,6 +376,17 @@ def run_ours(args, rank: int, world: int, local_rank: int):
 
     pk = peaks()
     flops_step = 8.0 * N * V * H
+    skip_info = None
+    if args.skip_ignored:
+        rows = 128 if args.single_cta else 256
+        nblk = (N + rows - 1) // rows
+        lab = np.full(nblk * rows, spec.ignore_index, dtype=np.int64)
+        lab[:N] = wl.labels
+        active = np.any(lab.reshape(nblk, rows) != spec.ignore_index, axis=1)
+        frac = float(np.minimum(rows, N - np.arange(nblk) * rows)[active].sum()) / N
+        skip_info = {"block_rows": rows, "active_token_fraction": frac,
+                     "note": "value counts all N tokens; tflops counts 8NVH over all N tokens "
+                             "(dense-equivalent); tflops_executed counts only active blocks"}
     tflops = flops_step / (ms_per_step / 1e3) / 1e12
     # algorithmic bytes of one step: X, W read; dX, dW written; labels, lse
     elem = 2 if spec.dtype == "bf16" else 4
@@ -422,8 +437,11 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                        parallelism=f"replicas x{world} (each rank its own batch, no collective)",
                        tiles="128x256 single CTA" if args.single_cta else "256x256 CTA pair",
                        z_loss=args.z_loss,
+                       skip_ignored_blocks=args.skip_ignored,
                        l2_hints=args.l2_hints),
         "tflops": tflops,
+        "skip": skip_info,
+        "tflops_executed": tflops * skip_info["active_token_fraction"] if skip_info else tflops,
         "step_roofline": {"bound": "tensor" if t_tensor >= t_hbm else "hbm",
                           "frac": step_frac, "flops": flops_step, "bytes": bytes_step,
                           "peak_tflops": pk["bf16_sustained"], "peak_source": pk["source"]},
