@@ -52,6 +52,9 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--l2-hints", action="store_true",
                     help="evict_last L2 policy for the operand re-read on every wave of tiles")
+    ap.add_argument("--vocab-shards", type=int, default=0,
+                    help="time the vocabulary-parallel layout with this many shards run one "
+                         "after another on the GPU (stack / sum stand in for the exchange)")
     ap.add_argument("--skip-ignored", action="store_true",
                     help="skip token blocks whose labels are all ignore_index")
     ap.add_argument("--z-loss", type=float, default=0.0,
@@ -249,12 +252,41 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     base_mem = torch.cuda.memory_allocated(dev)  # inputs and outputs only
     ws = B.workspace(N, H, V, dt, B.MODE_FWD_BWD, dev)
 
-    def step():
-        B.flce_fwd_bwd(X, W, y, spec.ignore_index, spec.smoothing, spec.reduction, loss=loss,
-                       lse=lse, valid_count=nv, dX=dX, dW=dW, workspace_buf=ws, err_word=err,
-                       stream=stream, z_loss=args.z_loss,
-                       skip_ignored_blocks=args.skip_ignored)
-        return B.last_launch_count()
+    if args.vocab_shards > 1:
+        P = args.vocab_shards
+        bounds = [round(V * i / P / 256) * 256 for i in range(P)] + [V]
+        opt = B.make_options(spec.ignore_index, spec.smoothing, spec.reduction, args.z_loss)
+        max_vs = max(b1 - b0 for b0, b1 in zip(bounds, bounds[1:]))
+        ws = B.workspace(N, H, max_vs, dt, B.MODE_FWD_BWD, dev)
+        parts = torch.empty(P, N, 4, dtype=torch.float32, device=dev)
+        dxp = [torch.empty(N, H, dtype=torch.float32, device=dev) for _ in range(P)]
+        dXf = torch.empty(N, H, dtype=torch.float32, device=dev)
+
+        def step():
+            n = 0
+            for i, (b0, b1) in enumerate(zip(bounds, bounds[1:])):
+                B.flce_forward_vocab_shard(X, W[b0:b1], y, b0, V, opt, partials=parts[i],
+                                           workspace_buf=ws, err_word=err, stream=stream)
+                n += B.last_launch_count()
+            B.flce_combine_vocab_shards(parts, y, V, opt, loss=loss, lse=lse, valid_count=nv,
+                                        err_word=err, stream=stream)
+            n += B.last_launch_count()
+            for i, (b0, b1) in enumerate(zip(bounds, bounds[1:])):
+                B.flce_backward_vocab_shard(X, W[b0:b1], y, b0, V, lse, nv, opt,
+                                            dX_partial=dxp[i], dW_shard=dW[b0:b1],
+                                            workspace_buf=ws, err_word=err, stream=stream)
+                n += B.last_launch_count()
+            torch.sum(torch.stack(dxp), dim=0, out=dXf)  # stands in for the all-reduce
+            return n
+    else:
+        def step():
+            B.flce_fwd_bwd(X, W, y, spec.ignore_index, spec.smoothing, spec.reduction, loss=loss,
+                           lse=lse, valid_count=nv, dX=dX, dW=dW, workspace_buf=ws, err_word=err,
+                           stream=stream, z_loss=args.z_loss,
+                           skip_ignored_blocks=args.skip_ignored)
+            return B.last_launch_count()
+    if args.vocab_shards > 1:
+        args.no_e2e = True  # the end-to-end leg times the unsharded call only
 
     for _ in range(max(args.warmup, 0)):
         step()
@@ -438,6 +470,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                        tiles="128x256 single CTA" if args.single_cta else "256x256 CTA pair",
                        z_loss=args.z_loss,
                        skip_ignored_blocks=args.skip_ignored,
+                       vocab_shards=args.vocab_shards or None,
                        l2_hints=args.l2_hints),
         "tflops": tflops,
         "skip": skip_info,

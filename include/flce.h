@@ -187,6 +187,47 @@ flce_status flce_fwd_bwd_ex(const void* X, const void* W, const int64_t* labels,
                             int32_t* valid_count, void* dX, float* dW, int accumulate_dW,
                             void* workspace, size_t ws_bytes, int32_t* err_word, void* stream);
 
+/* Vocabulary-parallel layout (the "tiled vocabulary dot
+ * products" of "Chunked and Fused Cross-Entropy ...", comparison table, with
+ * step 2's running (m, d) carried across vocabulary shards).  Shard p holds
+ * rows [vocab_offset, vocab_offset + V_shard) of W for a vocabulary of
+ * vocab_total; labels stay global.  A step is:
+ *   1. every shard: flce_forward_vocab_shard -> partials (device float[N][4]:
+ *      max * log2(e), sum of exp(z - max) rescaled, the target logit if the
+ *      label is in this shard else 0, the shard's row sum of logits);
+ *   2. gather the P shards' partials into one device float[P][N][4] (the
+ *      exchange, e.g. an all-gather of N * 16 bytes per shard) and call
+ *      flce_combine_vocab_shards -> loss, lse, valid_count (the LSE-combine);
+ *   3. every shard: flce_backward_vocab_shard with the global lse and
+ *      valid_count -> its fp32 partial dX (N x H; the shards' partials sum to
+ *      dX: an all-reduce) and its own dW rows (V_shard x H fp32).
+ * opt: ignore_index, smoothing (eps / vocab_total per class), z_loss,
+ * reduction; row_loss only in the combine; skip_ignored_blocks must be 0.
+ * Workspaces: flce_workspace_size(N, H, V_shard, dtype, FLCE_MODE_FWD / _BWD)
+ * for the shard calls, flce_combine_workspace_size(N) for the combine. */
+flce_status flce_forward_vocab_shard(const void* X, const void* W_shard, const int64_t* labels,
+                                     int64_t N, int64_t H, int64_t V_shard, int64_t vocab_offset,
+                                     int64_t vocab_total, flce_dtype dtype,
+                                     const flce_options* opt, float* partials, void* workspace,
+                                     size_t ws_bytes, int32_t* err_word, void* stream);
+
+size_t flce_combine_workspace_size(int64_t N);
+
+flce_status flce_combine_vocab_shards(const float* partials, int n_shards, int64_t N,
+                                      const int64_t* labels, int64_t vocab_total,
+                                      const flce_options* opt, float* loss, float* lse,
+                                      int32_t* valid_count, void* workspace, size_t ws_bytes,
+                                      int32_t* err_word, void* stream);
+
+flce_status flce_backward_vocab_shard(const void* X, const void* W_shard, const int64_t* labels,
+                                      int64_t N, int64_t H, int64_t V_shard,
+                                      int64_t vocab_offset, int64_t vocab_total,
+                                      flce_dtype dtype, const flce_options* opt,
+                                      const float* lse, const int32_t* valid_count,
+                                      const float* grad_loss, float* dX_partial,
+                                      float* dW_shard, int accumulate_dW, void* workspace,
+                                      size_t ws_bytes, int32_t* err_word, void* stream);
+
 /* Human-readable name of a status code (static string). */
 const char* flce_status_string(flce_status s);
 

@@ -37,7 +37,8 @@ EXPORTED = (
     "flce_last_launch_count", "flce_abi_version", "flce_debug_gemm", "flce_profile_enable",
     "flce_profile_read", "flce_profile_reset", "flce_forward_noalloc", "flce_noalloc_last_error",
     "flce_set_cta_pair", "flce_cta_pair", "flce_set_l2_hints", "flce_options_init",
-    "flce_forward_ex", "flce_backward_ex", "flce_fwd_bwd_ex",
+    "flce_forward_ex", "flce_backward_ex", "flce_fwd_bwd_ex", "flce_forward_vocab_shard",
+    "flce_combine_workspace_size", "flce_combine_vocab_shards", "flce_backward_vocab_shard",
 )
 
 PROFILE_KINDS = ("fwd_logits_lse", "bwd_dz_recompute", "bwd_dw_gemm", "bwd_dx_gemm")
@@ -124,6 +125,16 @@ def lib() -> ctypes.CDLL:
     L.flce_fwd_bwd_ex.argtypes = [P, P, P, I64, I64, I64, I32, OPT, P, P, P, P, P, P, I32, P, SZ,
                                   P, P]
     L.flce_fwd_bwd_ex.restype = I32
+    L.flce_forward_vocab_shard.argtypes = [P, P, P, I64, I64, I64, I64, I64, I32, OPT, P, P, SZ,
+                                           P, P]
+    L.flce_forward_vocab_shard.restype = I32
+    L.flce_combine_workspace_size.argtypes = [I64]
+    L.flce_combine_workspace_size.restype = SZ
+    L.flce_combine_vocab_shards.argtypes = [P, I32, I64, P, I64, OPT, P, P, P, P, SZ, P, P]
+    L.flce_combine_vocab_shards.restype = I32
+    L.flce_backward_vocab_shard.argtypes = [P, P, P, I64, I64, I64, I64, I64, I32, OPT, P, P, P,
+                                            P, P, I32, P, SZ, P, P]
+    L.flce_backward_vocab_shard.restype = I32
     _lib = L
     return L
 
@@ -373,6 +384,67 @@ def flce_fwd_bwd_ex(X, W, labels, options: FlceOptions, *, grad_loss=None, loss=
                                ws.numel(), _ptr(err_word), _stream(stream))
     _check(st, "flce_fwd_bwd_ex")
     return loss, lse, valid_count, dX, dW, err_word
+
+
+def flce_forward_vocab_shard(X, W_shard, labels, vocab_offset: int, vocab_total: int,
+                             options: FlceOptions = None, *, partials=None, workspace_buf=None,
+                             err_word=None, stream=None):
+    """This shard's per-row partial statistics, a float32 [N, 4] tensor."""
+    N, H, Vs = _check_inputs(X, W_shard, labels)
+    dev = X.device
+    dt = _dtype_code(X)
+    options = make_options() if options is None else options
+    partials = torch.empty(N, 4, dtype=torch.float32, device=dev) if partials is None else partials
+    ws = workspace(N, H, Vs, dt, MODE_FWD, dev) if workspace_buf is None else workspace_buf
+    err_word = new_err_word(dev) if err_word is None else err_word
+    st = lib().flce_forward_vocab_shard(_ptr(X), _ptr(W_shard), _ptr(labels), N, H, Vs,
+                                        vocab_offset, vocab_total, dt, ctypes.byref(options),
+                                        _ptr(partials), _ptr(ws), ws.numel(), _ptr(err_word),
+                                        _stream(stream))
+    _check(st, "flce_forward_vocab_shard")
+    return partials, err_word
+
+
+def flce_combine_vocab_shards(partials, labels, vocab_total: int, options: FlceOptions = None, *,
+                              loss=None, lse=None, valid_count=None, err_word=None, stream=None):
+    """LSE-combine of P shards' partials (float32 [P, N, 4]) -> (loss, lse, valid_count, err)."""
+    n_shards, N = partials.shape[0], partials.shape[1]
+    dev = partials.device
+    options = make_options() if options is None else options
+    loss = torch.empty(1, dtype=torch.float32, device=dev) if loss is None else loss
+    lse = torch.empty(N, dtype=torch.float32, device=dev) if lse is None else lse
+    valid_count = torch.empty(1, dtype=torch.int32, device=dev) if valid_count is None else valid_count
+    n = max(int(lib().flce_combine_workspace_size(N)), 256)
+    ws = torch.empty(n, dtype=torch.uint8, device=dev)
+    err_word = new_err_word(dev) if err_word is None else err_word
+    st = lib().flce_combine_vocab_shards(_ptr(partials.contiguous()), n_shards, N, _ptr(labels),
+                                         vocab_total, ctypes.byref(options), _ptr(loss), _ptr(lse),
+                                         _ptr(valid_count), _ptr(ws), ws.numel(), _ptr(err_word),
+                                         _stream(stream))
+    _check(st, "flce_combine_vocab_shards")
+    return loss, lse, valid_count, err_word
+
+
+def flce_backward_vocab_shard(X, W_shard, labels, vocab_offset: int, vocab_total: int, lse,
+                              valid_count, options: FlceOptions = None, *, grad_loss=None,
+                              dX_partial=None, dW_shard=None, accumulate_dW: bool = False,
+                              workspace_buf=None, err_word=None, stream=None):
+    """(fp32 partial dX [N, H], dW rows of this shard [V_shard, H] fp32, err)."""
+    N, H, Vs = _check_inputs(X, W_shard, labels)
+    dev = X.device
+    dt = _dtype_code(X)
+    options = make_options() if options is None else options
+    dX_partial = torch.empty(N, H, dtype=torch.float32, device=dev) if dX_partial is None else dX_partial
+    dW_shard = torch.empty(Vs, H, dtype=torch.float32, device=dev) if dW_shard is None else dW_shard
+    ws = workspace(N, H, Vs, dt, MODE_BWD, dev) if workspace_buf is None else workspace_buf
+    err_word = new_err_word(dev) if err_word is None else err_word
+    st = lib().flce_backward_vocab_shard(_ptr(X), _ptr(W_shard), _ptr(labels), N, H, Vs,
+                                         vocab_offset, vocab_total, dt, ctypes.byref(options),
+                                         _ptr(lse), _ptr(valid_count), _ptr(grad_loss),
+                                         _ptr(dX_partial), _ptr(dW_shard), int(bool(accumulate_dW)),
+                                         _ptr(ws), ws.numel(), _ptr(err_word), _stream(stream))
+    _check(st, "flce_backward_vocab_shard")
+    return dX_partial, dW_shard, err_word
 
 
 def flce_debug_gemm(A, B, M: int, Nn: int, K: int, a_mn: bool, b_mn: bool, D=None,

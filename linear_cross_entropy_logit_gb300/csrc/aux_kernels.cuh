@@ -78,6 +78,26 @@ static __global__ void __launch_bounds__(MERGE_THREADS)
   }
 }
 
+// One thread per token row: merge the vocabulary-group partials of ONE
+// vocabulary shard into a single (max*log2e, rescaled sum, z_y, sum_z) per
+// row -- the statistic shards exchange in the vocabulary-parallel layout.
+static __global__ void __launch_bounds__(MERGE_THREADS)
+    shard_partial_kernel(const float4* __restrict__ partials, int n_groups, int m_pad, int N,
+                         float4* __restrict__ out) {
+  const int row = blockIdx.x * MERGE_THREADS + threadIdx.x;
+  if (row >= N) return;
+  float M = -INFINITY;
+  for (int g = 0; g < n_groups; ++g) M = fmaxf(M, partials[(size_t)g * m_pad + row].x);
+  float S = 0.f, zy = 0.f, zs = 0.f;
+  for (int g = 0; g < n_groups; ++g) {
+    const float4 q = partials[(size_t)g * m_pad + row];
+    S += q.y * ex2_approx(q.x - M);
+    zy += q.z;
+    zs += q.w;
+  }
+  out[row] = make_float4(M, S, zy, zs);
+}
+
 // Single block: fixed-order sum of the block partials, then the mean over
 // valid tokens (0 when none are valid: the chunked reference divides by
 // max(valid_token_count, 1)) or the plain sum.

@@ -364,6 +364,11 @@ struct Common {
   size_t ws_bytes;
   int32_t* err_word;
   cudaStream_t st;
+  // vocabulary-parallel shards: W holds rows [vocab_offset, vocab_offset + V)
+  // of a vocabulary of vocab_total; the backward then returns an fp32 partial dX
+  int64_t vocab_offset = 0;
+  int64_t vocab_total = 0;
+  bool dx_partial_f32 = false;
 };
 
 flce_status validate_common(const Common& c, int mode, Plan* pl) {
@@ -440,7 +445,8 @@ flce_status cast_inputs(const Common& c, const Plan& pl, const void** Xb, const 
 }
 
 flce_status run_forward(const Common& c, const Plan& pl, int dev, int sms, const void* Xb,
-                        const void* Wb, float* loss, float* lse, int32_t* valid_count) {
+                        const void* Wb, float* loss, float* lse, int32_t* valid_count,
+                        float4* shard_out = nullptr) {
   uint8_t* ws = static_cast<uint8_t*>(c.ws);
   double* block_loss = reinterpret_cast<double*>(ws + pl.off_block_loss);
   int* block_valid = reinterpret_cast<int*>(ws + pl.off_block_valid);
@@ -463,8 +469,8 @@ flce_status run_forward(const Common& c, const Plan& pl, int dev, int sms, const
     p.m_fastest = 1;
     p.labels = c.labels;
     p.ignore_index = c.ignore_index;
-    p.vocab = (int)c.V;
-    p.col_base = 0;
+    p.vocab = (int)c.vocab_total;
+    p.col_base = (int)c.vocab_offset;
     p.col_limit = (int)c.V;
     p.smoothing = c.smoothing;
     p.partials = reinterpret_cast<float4*>(ws + pl.off_partials);
@@ -476,6 +482,14 @@ flce_status run_forward(const Common& c, const Plan& pl, int dev, int sms, const
     p.err_word = c.err_word;
     p.timeout_ns = kTimeoutNs;
     FLCE_TRY((launch_tile<Epi::kLse, false, false>(pair, dev, sms, tmX, tmW, tmX, p, c.st, 0)));
+    if (shard_out) {
+      // vocabulary shard: one merged partial per row, no loss yet
+      shard_partial_kernel<<<pl.merge_blocks, MERGE_THREADS, 0, c.st>>>(
+          p.partials, pl.n_groups, pl.m_pad, (int)c.N, shard_out);
+      ++g_launches;
+      FLCE_CUDA(cudaGetLastError());
+      return FLCE_OK;
+    }
     lse_merge_kernel<<<pl.merge_blocks, MERGE_THREADS, 0, c.st>>>(
         p.partials, pl.n_groups, pl.m_pad, (int)c.N, (int)c.V, c.labels, c.ignore_index,
         c.smoothing, c.z_loss, lse, c.row_loss, block_loss, block_valid, c.err_word, sk.flags,
@@ -505,8 +519,9 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
   }
   const int64_t N = c.N, H = c.H, V = c.V, Cv = pl.chunk;
   void* dz = ws + pl.off_dz;
-  float* dx_acc = c.dtype == FLCE_BF16 ? reinterpret_cast<float*>(ws + pl.off_dxacc)
-                                       : static_cast<float*>(dX);
+  float* dx_acc = (c.dtype == FLCE_BF16 && !c.dx_partial_f32)
+                      ? reinterpret_cast<float*>(ws + pl.off_dxacc)
+                      : static_cast<float*>(dX);
   const auto* Wb16 = static_cast<const uint16_t*>(Wb);
 
   CUtensorMap tmX_k, tmX_mn, tmDxAcc;
@@ -550,8 +565,8 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
     p3.m_fastest = 1;
     p3.labels = c.labels;
     p3.ignore_index = c.ignore_index;
-    p3.vocab = (int)V;
-    p3.col_base = (int)v0;
+    p3.vocab = (int)c.vocab_total;
+    p3.col_base = (int)(c.vocab_offset + v0);
     p3.col_limit = (int)w;
     p3.smoothing = c.smoothing;
     p3.z_loss = c.z_loss;
@@ -606,7 +621,7 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
     p5.timeout_ns = kTimeoutNs;
     FLCE_TRY((launch_tile<Epi::kStore, false, true>(pair, dev, sms, tmDz_k, tmWc_mn, tmDxAcc, p5, c.st, 3)));
   }
-  if (c.dtype == FLCE_BF16) {
+  if (c.dtype == FLCE_BF16 && !c.dx_partial_f32) {
     const size_t n4 = (size_t)N * H / 4;
     dx_finalize_bf16_kernel<<<(unsigned)std::min<size_t>(ceil_div(n4, 256), 2 * sms), 256, 0,
                               c.st>>>(reinterpret_cast<const float4*>(dx_acc),
@@ -744,7 +759,10 @@ Common make_common(const void* X, const void* W, const int64_t* labels, int64_t 
                 ws,
                 ws_bytes,
                 err_word,
-                static_cast<cudaStream_t>(stream)};
+                static_cast<cudaStream_t>(stream),
+                0,
+                V,
+                false};
 }
 
 flce_options defaults(int64_t ignore_index, float smoothing, flce_reduction reduction) {
@@ -848,6 +866,127 @@ flce_status flce_fwd_bwd(const void* X, const void* W, const int64_t* labels, in
   const flce_options o = defaults(ignore_index, smoothing, reduction);
   return flce_fwd_bwd_ex(X, W, labels, N, H, V, dtype, &o, grad_loss, loss, lse, valid_count, dX,
                          dW, accumulate_dW, workspace, ws_bytes, err_word, stream);
+}
+
+// ---------------------------------------------------------------------------
+// Vocabulary-parallel shards
+// ---------------------------------------------------------------------------
+}  // extern "C"
+
+namespace {
+
+flce_status shard_common(const void* X, const void* W_shard, const int64_t* labels, int64_t N,
+                         int64_t H, int64_t V_shard, int64_t vocab_offset, int64_t vocab_total,
+                         flce_dtype dtype, const flce_options* opt, void* ws, size_t ws_bytes,
+                         int32_t* err_word, void* stream, Common* out) {
+  if (!options_ok(opt)) return FLCE_ERR_ARG;
+  if (opt->skip_ignored_blocks || opt->row_loss) return FLCE_ERR_ARG;
+  if (vocab_offset < 0 || V_shard <= 0 || vocab_total < vocab_offset + V_shard ||
+      vocab_total > (int64_t)INT32_MAX - 1024)
+    return FLCE_ERR_ARG;
+  *out = make_common(X, W_shard, labels, N, H, V_shard, dtype, opt, ws, ws_bytes, err_word,
+                     stream);
+  out->vocab_offset = vocab_offset;
+  out->vocab_total = vocab_total;
+  return FLCE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+flce_status flce_forward_vocab_shard(const void* X, const void* W_shard, const int64_t* labels,
+                                     int64_t N, int64_t H, int64_t V_shard, int64_t vocab_offset,
+                                     int64_t vocab_total, flce_dtype dtype,
+                                     const flce_options* opt, float* partials, void* workspace,
+                                     size_t ws_bytes, int32_t* err_word, void* stream) {
+  g_launches = 0;
+  Common c;
+  FLCE_TRY(shard_common(X, W_shard, labels, N, H, V_shard, vocab_offset, vocab_total, dtype, opt,
+                        workspace, ws_bytes, err_word, stream, &c));
+  Plan pl;
+  FLCE_TRY(validate_common(c, FLCE_MODE_FWD, &pl));
+  if (N > 0 && (!partials || !aligned(partials, 16))) return FLCE_ERR_ARG;
+  if (N == 0) return FLCE_OK;
+  int dev, sms;
+  FLCE_TRY(device_check(&dev, &sms));
+  const void *Xb, *Wb;
+  FLCE_TRY(cast_inputs(c, pl, &Xb, &Wb));
+  return run_forward(c, pl, dev, sms, Xb, Wb, nullptr, nullptr, nullptr,
+                     reinterpret_cast<float4*>(partials));
+}
+
+size_t flce_combine_workspace_size(int64_t N) {
+  if (N < 0) return 0;
+  const size_t nb = (size_t)ceil_div(std::max<int64_t>(N, 1), MERGE_THREADS);
+  return align_up(nb * sizeof(double), kAlign) + align_up(nb * sizeof(int), kAlign);
+}
+
+flce_status flce_combine_vocab_shards(const float* partials, int n_shards, int64_t N,
+                                      const int64_t* labels, int64_t vocab_total,
+                                      const flce_options* opt, float* loss, float* lse,
+                                      int32_t* valid_count, void* workspace, size_t ws_bytes,
+                                      int32_t* err_word, void* stream) {
+  g_launches = 0;
+  if (!options_ok(opt) || opt->skip_ignored_blocks) return FLCE_ERR_ARG;
+  if (n_shards <= 0 || N < 0 || N > (int64_t)INT32_MAX - 1024 || vocab_total <= 0 ||
+      vocab_total > (int64_t)INT32_MAX - 1024)
+    return FLCE_ERR_ARG;
+  if (opt->reduction != FLCE_MEAN && opt->reduction != FLCE_SUM) return FLCE_ERR_ARG;
+  if (!(opt->smoothing >= 0.f && opt->smoothing < 1.f) || !(opt->z_loss >= 0.f))
+    return FLCE_ERR_ARG;
+  if (!loss || !valid_count || !err_word) return FLCE_ERR_ARG;
+  if (N > 0 && (!partials || !labels || !lse || !aligned(partials, 16))) return FLCE_ERR_ARG;
+  if (opt->row_loss && !aligned(opt->row_loss, 4)) return FLCE_ERR_ARG;
+  if (!workspace || !aligned(workspace, kAlign) || ws_bytes < flce_combine_workspace_size(N))
+    return FLCE_ERR_WORKSPACE;
+  int dev, sms;
+  FLCE_TRY(device_check(&dev, &sms));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int nb = (int)ceil_div(std::max<int64_t>(N, 1), MERGE_THREADS);
+  double* block_loss = static_cast<double*>(workspace);
+  int* block_valid = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) +
+                                            align_up(nb * sizeof(double), kAlign));
+  if (N > 0) {
+    // the LSE-combine of the shards is the merge of n_shards partials per row
+    lse_merge_kernel<<<nb, MERGE_THREADS, 0, st>>>(
+        reinterpret_cast<const float4*>(partials), n_shards, (int)N, (int)N, (int)vocab_total,
+        labels, opt->ignore_index, opt->smoothing, opt->z_loss, lse, opt->row_loss, block_loss,
+        block_valid, err_word, nullptr, 1);
+    ++g_launches;
+    FLCE_CUDA(cudaGetLastError());
+  }
+  loss_finalize_kernel<<<1, MERGE_THREADS, 0, st>>>(block_loss, block_valid, N > 0 ? nb : 0,
+                                                     opt->reduction == FLCE_SUM, loss,
+                                                     valid_count);
+  ++g_launches;
+  FLCE_CUDA(cudaGetLastError());
+  return FLCE_OK;
+}
+
+flce_status flce_backward_vocab_shard(const void* X, const void* W_shard, const int64_t* labels,
+                                      int64_t N, int64_t H, int64_t V_shard,
+                                      int64_t vocab_offset, int64_t vocab_total,
+                                      flce_dtype dtype, const flce_options* opt,
+                                      const float* lse, const int32_t* valid_count,
+                                      const float* grad_loss, float* dX_partial,
+                                      float* dW_shard, int accumulate_dW, void* workspace,
+                                      size_t ws_bytes, int32_t* err_word, void* stream) {
+  g_launches = 0;
+  Common c;
+  FLCE_TRY(shard_common(X, W_shard, labels, N, H, V_shard, vocab_offset, vocab_total, dtype, opt,
+                        workspace, ws_bytes, err_word, stream, &c));
+  c.dx_partial_f32 = true;
+  Plan pl;
+  FLCE_TRY(validate_common(c, FLCE_MODE_BWD, &pl));
+  if (!valid_count || !dW_shard || !aligned(dW_shard, 16)) return FLCE_ERR_ARG;
+  if (N > 0 && (!lse || !dX_partial || !aligned(dX_partial, 16))) return FLCE_ERR_ARG;
+  int dev, sms;
+  FLCE_TRY(device_check(&dev, &sms));
+  const void *Xb, *Wb;
+  FLCE_TRY(cast_inputs(c, pl, &Xb, &Wb));
+  return run_backward(c, pl, dev, sms, Xb, Wb, lse, valid_count, grad_loss, dX_partial, dW_shard,
+                      accumulate_dW);
 }
 
 flce_status flce_debug_gemm(const void* A, const void* B, float* D, int64_t M, int64_t Nn,

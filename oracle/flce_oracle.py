@@ -284,3 +284,69 @@ def fwd_bwd(X, W, labels, ignore_index: int = IGNORE_INDEX, smoothing: float = 0
     b = backward(X, W, labels, ignore_index, smoothing, reduction, grad_loss, dW_in,
                  z_loss=z_loss)
     return f, b
+
+
+# ----------------------------------------------------------------------------
+# Vocabulary-parallel decomposition ([CFCE] step 2's running (m, d) carried
+# across vocabulary shards instead of tiles; [CFCE] comparison table:
+# "Tiled vocabulary dot products").  Shard p holds W rows [v0, v0 + V_p) of a
+# vocabulary of V_total; labels stay global.
+# ----------------------------------------------------------------------------
+def shard_partials(X, W_shard, labels, v0: int, V_total: int,
+                   ignore_index: int = IGNORE_INDEX):
+    """Per-row (m, d, z_y, sum_z) of this shard: m = max over the shard's
+    logits, d = sum exp(z - m), z_y = the target logit if y_i lies in the
+    shard (else 0), sum_z = the shard's row sum of logits."""
+    Z = upcast(X) @ upcast(W_shard).T
+    m = Z.max(axis=1)
+    d = np.exp(Z - m[:, None]).sum(axis=1)
+    labels = np.asarray(labels, dtype=np.int64)
+    rel = labels - v0
+    mine = (labels != ignore_index) & (rel >= 0) & (rel < Z.shape[1])
+    z_y = np.zeros(Z.shape[0])
+    rows = np.flatnonzero(mine)
+    z_y[rows] = Z[rows, rel[rows]]
+    return m, d, z_y, Z.sum(axis=1)
+
+
+def combine_partials(parts, labels, V_total: int, ignore_index: int = IGNORE_INDEX,
+                     smoothing: float = 0.0, reduction: str = "mean", z_loss: float = 0.0):
+    """LSE-combine of the shards' (m, d, z_y, sum_z): M = max_p m_p,
+    lse = M + log sum_p d_p exp(m_p - M); z_y and sum_z add up.  Returns
+    (loss, lse, row_loss, n_valid) with the same loss as ``forward``."""
+    m = np.stack([p[0] for p in parts])
+    d = np.stack([p[1] for p in parts])
+    M = m.max(axis=0)
+    lse = M + np.log((d * np.exp(m - M)).sum(axis=0))
+    z_y = sum(p[2] for p in parts)
+    zs = sum(p[3] for p in parts)
+    labels = np.asarray(labels, dtype=np.int64)
+    valid = valid_mask(labels, V_total, ignore_index)
+    row = lse - (1.0 - smoothing) * z_y - (smoothing / V_total) * zs + z_loss * lse * lse
+    row = np.where(valid, row, 0.0)
+    nv = int(valid.sum())
+    total = float(row.sum())
+    loss = total if reduction == "sum" else (total / nv if nv else 0.0)
+    return loss, lse, row, nv
+
+
+def shard_backward(X, W_shard, labels, v0: int, V_total: int, lse: np.ndarray, c: float,
+                   ignore_index: int = IGNORE_INDEX, smoothing: float = 0.0,
+                   z_loss: float = 0.0):
+    """This shard's dZ columns (global lse, eps / V_total), its partial
+    dX = dZ_p W_p (to be summed over shards) and its dW rows."""
+    Xd, Wd = upcast(X), upcast(W_shard)
+    Z = Xd @ Wd.T
+    labels = np.asarray(labels, dtype=np.int64)
+    valid = valid_mask(labels, V_total, ignore_index)
+    P = np.exp(Z - lse[:, None])
+    if z_loss != 0.0:
+        P = P * (1.0 + 2.0 * z_loss * lse)[:, None]
+    dZ = P - smoothing / V_total
+    rel = labels - v0
+    hit = valid & (rel >= 0) & (rel < Z.shape[1])
+    rows = np.flatnonzero(hit)
+    dZ[rows, rel[rows]] -= (1.0 - smoothing)
+    dZ[~valid] = 0.0
+    dZ *= c
+    return dZ @ Wd, dZ.T @ Xd

@@ -422,3 +422,35 @@ def test_z_loss_against_torch():
     assert np.allclose(O.dx_rows(X, W, y, rows, c, IGN, eps, a), b.dX[rows], atol=1e-14)
     assert np.allclose(O.dw_rows(X, W, y, [1, 7], f.lse, c, IGN, eps, a), b.dW[[1, 7]],
                        atol=1e-14)
+
+
+# --------------------------------------------------------------------------
+# Vocabulary shards compose to the unsharded definition
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("bounds", [[0, 7, 19, 31], [0, 1, 30, 31]])
+def test_vocab_shards_compose(bounds):
+    N, H, V, eps, a = 11, 6, 31, 0.1, 0.01
+    X, W, y = rand_case(N, H, V, 33, n_ignore=3)
+    f, b = O.fwd_bwd(X, W, y, IGN, eps, "mean", z_loss=a)
+    parts = [O.shard_partials(X, W[v0:v1], y, v0, V, IGN) for v0, v1 in zip(bounds, bounds[1:])]
+    loss, lse, row, nv = O.combine_partials(parts, y, V, IGN, eps, "mean", a)
+    assert loss == pytest.approx(f.loss, abs=1e-13)
+    assert np.allclose(lse, f.lse, atol=1e-13) and np.allclose(row, f.row_loss, atol=1e-13)
+    assert nv == f.n_valid
+    c = 1.0 / nv
+    dX = np.zeros_like(b.dX)
+    dW = []
+    for v0, v1 in zip(bounds, bounds[1:]):
+        dx_p, dw_p = O.shard_backward(X, W[v0:v1], y, v0, V, lse, c, IGN, eps, a)
+        dX += dx_p
+        dW.append(dw_p)
+    assert np.allclose(dX, b.dX, atol=1e-14)
+    assert np.allclose(np.concatenate(dW), b.dW, atol=1e-14)
+
+
+def test_shard_partial_closed_form():
+    """A shard with W = 0 has m = 0, d = V_p, z_y = 0 and sum_z = 0."""
+    X, _, y = rand_case(4, 3, 10, 34)
+    m, d, zy, zs = O.shard_partials(X, np.zeros((4, 3)), y, 6, 10)
+    assert np.all(m == 0) and np.all(d == 4) and np.all(zs == 0)
+    assert np.all(zy == 0)
