@@ -274,6 +274,14 @@ const char* flce_noalloc_last_error(void);
 /* ABI version of this header (major * 100 + minor). */
 int flce_abi_version(void);
 
+/* TEST-ONLY: runs the library's bounded mbarrier wait (the one every pipeline
+ * wait of the GEMM kernels uses) on a barrier nothing arrives on, with a limit
+ * of timeout_ns (<= 10 s).  The kernel records FLCE_ERR_TIMEOUT in *err_word,
+ * writes the microseconds it waited to *waited_us (device int32) and returns,
+ * leaving the CUDA context usable. */
+flce_status flce_debug_wait_timeout(int32_t* err_word, uint64_t timeout_ns, int32_t* waited_us,
+                                    void* stream);
+
 /* TEST-ONLY: the library's tcgen05 GEMM core without a loss epilogue.
  * D (M x Nn fp32, device, row-major) = A * B^T, or += when accumulate != 0,
  * where A is M x K (a_mn = 0: stored M x K row-major) or stored K x M

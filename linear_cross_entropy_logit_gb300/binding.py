@@ -39,6 +39,7 @@ EXPORTED = (
     "flce_set_cta_pair", "flce_cta_pair", "flce_set_l2_hints", "flce_options_init",
     "flce_forward_ex", "flce_backward_ex", "flce_fwd_bwd_ex", "flce_forward_vocab_shard",
     "flce_combine_workspace_size", "flce_combine_vocab_shards", "flce_backward_vocab_shard",
+    "flce_debug_wait_timeout",
 )
 
 PROFILE_KINDS = ("fwd_logits_lse", "bwd_dz_recompute", "bwd_dw_gemm", "bwd_dx_gemm")
@@ -135,6 +136,8 @@ def lib() -> ctypes.CDLL:
     L.flce_backward_vocab_shard.argtypes = [P, P, P, I64, I64, I64, I64, I64, I32, OPT, P, P, P,
                                             P, P, I32, P, SZ, P, P]
     L.flce_backward_vocab_shard.restype = I32
+    L.flce_debug_wait_timeout.argtypes = [P, ctypes.c_uint64, P, P]
+    L.flce_debug_wait_timeout.restype = I32
     _lib = L
     return L
 

@@ -207,4 +207,25 @@ static __global__ void zero_skipped_rows_kernel(const int* __restrict__ flags, i
   }
 }
 
+// Test-only: one bounded wait on an mbarrier that nothing arrives on.  It must
+// give up after `timeout_ns`, record FLCE_ERR_TIMEOUT and return -- the path
+// every pipeline wait of the GEMM kernels takes when its partner never comes.
+static __global__ void wait_timeout_probe_kernel(int* err_word, unsigned long long timeout_ns,
+                                                 int* waited_out) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const WaitCtx ctx{&abort_flag, err_word, timeout_ns};
+    const uint64_t t0 = global_timer_ns();
+    const bool ok = mbar_wait(&bar, 0, ctx);
+    *waited_out = ok ? -1 : (int)((global_timer_ns() - t0) / 1000ull);  // microseconds
+  }
+}
+
 }  // namespace flce

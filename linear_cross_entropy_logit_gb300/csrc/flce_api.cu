@@ -989,6 +989,20 @@ flce_status flce_backward_vocab_shard(const void* X, const void* W_shard, const 
                       accumulate_dW);
 }
 
+flce_status flce_debug_wait_timeout(int32_t* err_word, uint64_t timeout_ns,
+                                    int32_t* waited_us, void* stream) {
+  g_launches = 0;
+  if (!err_word || !waited_us || timeout_ns == 0 || timeout_ns > 10000000000ull)
+    return FLCE_ERR_ARG;
+  int dev, sms;
+  FLCE_TRY(device_check(&dev, &sms));
+  wait_timeout_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(err_word, timeout_ns,
+                                                                             waited_us);
+  ++g_launches;
+  FLCE_CUDA(cudaGetLastError());
+  return FLCE_OK;
+}
+
 flce_status flce_debug_gemm(const void* A, const void* B, float* D, int64_t M, int64_t Nn,
                             int64_t K, int a_mn, int b_mn, int accumulate, int32_t* err_word,
                             void* stream) {
