@@ -55,6 +55,8 @@ def parse_args():
     ap.add_argument("--vocab-shards", type=int, default=0,
                     help="time the vocabulary-parallel layout with this many shards run one "
                          "after another on the GPU (stack / sum stand in for the exchange)")
+    ap.add_argument("--grad-filter", type=float, default=0.0,
+                    help="gradient filtering threshold eps_f (e.g. 2**-12; 0 = exact)")
     ap.add_argument("--skip-ignored", action="store_true",
                     help="skip token blocks whose labels are all ignore_index")
     ap.add_argument("--z-loss", type=float, default=0.0,
@@ -283,7 +285,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             B.flce_fwd_bwd(X, W, y, spec.ignore_index, spec.smoothing, spec.reduction, loss=loss,
                            lse=lse, valid_count=nv, dX=dX, dW=dW, workspace_buf=ws, err_word=err,
                            stream=stream, z_loss=args.z_loss,
-                           skip_ignored_blocks=args.skip_ignored)
+                           skip_ignored_blocks=args.skip_ignored, grad_filter=args.grad_filter)
             return B.last_launch_count()
     if args.vocab_shards > 1:
         args.no_e2e = True  # the end-to-end leg times the unsharded call only
@@ -371,7 +373,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             B.flce_fwd_bwd(xd, wd, yd, spec.ignore_index, spec.smoothing, spec.reduction,
                            loss=lo, lse=ls, valid_count=sl["nv"], dX=dx, dW=dw,
                            workspace_buf=ws, err_word=err, stream=stream, z_loss=args.z_loss,
-                           skip_ignored_blocks=args.skip_ignored)
+                           skip_ignored_blocks=args.skip_ignored, grad_filter=args.grad_filter)
             sl["ev_comp"].record(stream)
             with torch.cuda.stream(s_down):
                 s_down.wait_event(sl["ev_comp"])
@@ -470,6 +472,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                        tiles="128x256 single CTA" if args.single_cta else "256x256 CTA pair",
                        z_loss=args.z_loss,
                        skip_ignored_blocks=args.skip_ignored,
+                       grad_filter=args.grad_filter or None,
                        vocab_shards=args.vocab_shards or None,
                        l2_hints=args.l2_hints),
         "tflops": tflops,

@@ -157,7 +157,17 @@ flce_status flce_fwd_bwd(const void* X, const void* W, const int64_t* labels, in
  *                 instruction tuning masks whole prompt spans ("Chunked and
  *                 Fused Cross-Entropy ...", "Numerical Considerations ...",
  *                 item 2).  loss, dX and dW are unchanged; lse of the rows of a
- *                 skipped block is NaN. */
+ *                 skipped block is NaN.
+ *   grad_filter   0 (default) or a threshold eps_f in (0, 1), e.g. 2^-12:
+ *                 gradient filtering after Cut Cross-Entropy ("Chunked and
+ *                 Fused Cross-Entropy ...", "Apple Cut Cross-Entropy (CCE)"):
+ *                 the dX and dW GEMMs skip every 32-token x 64-column block of
+ *                 dZ whose probabilities are all below eps_f and that holds no
+ *                 target.  An approximation: the dropped entries each have
+ *                 |dZ| <= c * max((1 + 2 alpha lse) eps_f, eps / V), so
+ *                 |delta dX|_F <= |delta dZ|_F |W|_2 and |delta dW|_F <=
+ *                 |delta dZ|_F |X|_2.  Needs ceil(Cv/64) and ceil(N/64) <= 1024
+ *                 (else FLCE_ERR_UNSUPPORTED); loss and lse are exact. */
 typedef struct flce_options {
   size_t struct_size;
   int64_t ignore_index;
@@ -166,6 +176,7 @@ typedef struct flce_options {
   flce_reduction reduction;
   float* row_loss;
   int skip_ignored_blocks;
+  float grad_filter;
 } flce_options;
 
 void flce_options_init(flce_options* opt);

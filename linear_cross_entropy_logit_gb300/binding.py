@@ -52,7 +52,7 @@ class FlceOptions(ctypes.Structure):
     _fields_ = [("struct_size", ctypes.c_size_t), ("ignore_index", ctypes.c_int64),
                 ("smoothing", ctypes.c_float), ("z_loss", ctypes.c_float),
                 ("reduction", ctypes.c_int), ("row_loss", ctypes.c_void_p),
-                ("skip_ignored_blocks", ctypes.c_int)]
+                ("skip_ignored_blocks", ctypes.c_int), ("grad_filter", ctypes.c_float)]
 
 
 class FlceError(RuntimeError):
@@ -224,7 +224,8 @@ def new_err_word(device) -> torch.Tensor:
 
 
 def make_options(ignore_index: int = -100, smoothing: float = 0.0, reduction: str = "mean",
-                 z_loss: float = 0.0, row_loss=None, skip_ignored_blocks: bool = False) -> FlceOptions:
+                 z_loss: float = 0.0, row_loss=None, skip_ignored_blocks: bool = False,
+                 grad_filter: float = 0.0) -> FlceOptions:
     o = FlceOptions()
     lib().flce_options_init(ctypes.byref(o))
     o.ignore_index = ignore_index
@@ -233,6 +234,7 @@ def make_options(ignore_index: int = -100, smoothing: float = 0.0, reduction: st
     o.reduction = _red_code(reduction)
     o.row_loss = _ptr(row_loss)
     o.skip_ignored_blocks = int(bool(skip_ignored_blocks))
+    o.grad_filter = grad_filter
     return o
 
 
@@ -283,13 +285,14 @@ def flce_backward(X, W, labels, lse, valid_count, ignore_index: int = -100,
                   smoothing: float = 0.0, reduction: str = "mean", *, grad_loss=None,
                   dX=None, dW=None, accumulate_dW: bool = False, workspace_buf=None,
                   err_word=None, stream=None, z_loss: float = 0.0,
-                  skip_ignored_blocks: bool = False):
+                  skip_ignored_blocks: bool = False, grad_filter: float = 0.0):
     """Returns (dX [N, H] in X's dtype, dW [V, H] fp32, err_word).
-    With z_loss or skip_ignored_blocks set it calls flce_backward_ex."""
-    if z_loss or skip_ignored_blocks:
+    With z_loss, skip_ignored_blocks or grad_filter set it calls flce_backward_ex."""
+    if z_loss or skip_ignored_blocks or grad_filter:
         return flce_backward_ex(X, W, labels, lse, valid_count,
                                 make_options(ignore_index, smoothing, reduction, z_loss,
-                                             skip_ignored_blocks=skip_ignored_blocks),
+                                             skip_ignored_blocks=skip_ignored_blocks,
+                                             grad_filter=grad_filter),
                                 grad_loss=grad_loss, dX=dX, dW=dW, accumulate_dW=accumulate_dW,
                                 workspace_buf=workspace_buf, err_word=err_word, stream=stream)
     N, H, V = _check_inputs(X, W, labels)
@@ -335,12 +338,13 @@ def flce_fwd_bwd(X, W, labels, ignore_index: int = -100, smoothing: float = 0.0,
                  reduction: str = "mean", *, grad_loss=None, loss=None, lse=None,
                  valid_count=None, dX=None, dW=None, accumulate_dW: bool = False,
                  workspace_buf=None, err_word=None, stream=None, z_loss: float = 0.0,
-                 row_loss=None, skip_ignored_blocks: bool = False):
+                 row_loss=None, skip_ignored_blocks: bool = False, grad_filter: float = 0.0):
     """Returns (loss, lse, valid_count, dX, dW, err_word).
-    With z_loss, row_loss or skip_ignored_blocks set it calls flce_fwd_bwd_ex."""
-    if z_loss or row_loss is not None or skip_ignored_blocks:
+    With z_loss, row_loss, skip_ignored_blocks or grad_filter set it calls flce_fwd_bwd_ex."""
+    if z_loss or row_loss is not None or skip_ignored_blocks or grad_filter:
         return flce_fwd_bwd_ex(X, W, labels, make_options(ignore_index, smoothing, reduction,
-                                                          z_loss, row_loss, skip_ignored_blocks),
+                                                          z_loss, row_loss, skip_ignored_blocks,
+                                                          grad_filter),
                                grad_loss=grad_loss, loss=loss, lse=lse, valid_count=valid_count,
                                dX=dX, dW=dW, accumulate_dW=accumulate_dW,
                                workspace_buf=workspace_buf, err_word=err_word, stream=stream)

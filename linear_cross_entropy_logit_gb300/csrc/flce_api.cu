@@ -95,7 +95,9 @@ struct Plan {
   int64_t chunk;
   int n_chunks;
   size_t off_scalars, off_blocks, off_partials, off_block_loss, off_block_valid, off_dz,
-      off_dxacc, off_xcast, off_wcast, total;
+      off_dxacc, off_xcast, off_wcast, off_mask_x, off_mask_w, total;
+  // gradient-filter masks (sized for 128-row tiles, the smaller tile shape)
+  int mask_x_ld, mask_w_ld;
   int n_blocks128;  // token blocks of 128 rows (the finest skip granularity)
 };
 
@@ -164,6 +166,12 @@ bool make_plan(int64_t N, int64_t H, int64_t V, flce_dtype dtype, int mode, Plan
       p.off_dxacc = off;
       off = align_up(off + (size_t)N * H * 4, kAlign);
     }
+    p.mask_x_ld = (int)align_up((size_t)ceil_div(p.chunk, BK), 16);
+    p.mask_w_ld = (int)align_up((size_t)ceil_div(std::max<int64_t>(N, 1), BK), 16);
+    p.off_mask_x = off;
+    off = align_up(off + (size_t)ceil_div(std::max<int64_t>(N, 1), BM) * p.mask_x_ld, kAlign);
+    p.off_mask_w = off;
+    off = align_up(off + (size_t)ceil_div(p.chunk, BM) * p.mask_w_ld, kAlign);
   }
   p.off_xcast = p.off_wcast = 0;
   if (dtype == FLCE_FP32) {
@@ -358,6 +366,7 @@ struct Common {
   float z_loss;
   float* row_loss;
   int skip_ignored;
+  float grad_filter;
   flce_dtype dtype;
   flce_reduction reduction;
   void* ws;
@@ -377,6 +386,7 @@ flce_status validate_common(const Common& c, int mode, Plan* pl) {
   if (c.reduction != FLCE_MEAN && c.reduction != FLCE_SUM) return FLCE_ERR_ARG;
   if (!(c.smoothing >= 0.f && c.smoothing < 1.f)) return FLCE_ERR_ARG;
   if (!(c.z_loss >= 0.f && c.z_loss < 1e30f)) return FLCE_ERR_ARG;
+  if (!(c.grad_filter >= 0.f && c.grad_filter < 1.f)) return FLCE_ERR_ARG;
   if (c.row_loss && !aligned(c.row_loss, 4)) return FLCE_ERR_ARG;
   if (!c.err_word) return FLCE_ERR_ARG;
   if (c.N > 0) {
@@ -540,9 +550,21 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
     FLCE_CUDA(cudaGetLastError());
   }
   const int h_blocks = (int)ceil_div(H, BN);
+  // gradient filtering: keep masks, one k-loop of a tile must fit the smem keep bytes
+  const bool filt = c.grad_filter > 0.f;
+  if (filt && (ceil_div(Cv, BK) > FILTER_MAX_KB || ceil_div(N, BK) > FILTER_MAX_KB))
+    return FLCE_ERR_UNSUPPORTED;
+  uint8_t* mask_x = ws + pl.off_mask_x;
+  uint8_t* mask_w = ws + pl.off_mask_w;
+  const size_t mask_x_bytes = (size_t)ceil_div(N, BM) * pl.mask_x_ld;
+  const size_t mask_w_bytes = (size_t)ceil_div(Cv, BM) * pl.mask_w_ld;
   for (int ci = 0; ci < pl.n_chunks; ++ci) {
     const int64_t v0 = (int64_t)ci * Cv;
     const int64_t w = std::min(Cv, V - v0);
+    if (filt) {
+      FLCE_CUDA(cudaMemsetAsync(mask_x, 0, mask_x_bytes, c.st));
+      FLCE_CUDA(cudaMemsetAsync(mask_w, 0, mask_w_bytes, c.st));
+    }
     const void* Wc = Wb16 + v0 * H;
     CUtensorMap tmWc_k, tmWc_mn, tmDzSt, tmDz_mn, tmDz_k, tmDw;
     FLCE_TRY(map_kmajor(&tmWc_k, Wc, H, w, H, b_box_rows(pair)));
@@ -572,6 +594,14 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
     p3.z_loss = c.z_loss;
     p3.row_list = sk.list;
     p3.row_count = sk.count;
+    if (filt) {
+      p3.mask_x_out = mask_x;
+      p3.mask_w_out = mask_w;
+      p3.mask_x_ld = pl.mask_x_ld;
+      p3.mask_w_ld = pl.mask_w_ld;
+      p3.mask_tile = tile_rows(pair);
+      p3.filter_thr = c.grad_filter;
+    }
     p3.lse = lse;
     p3.scale = scale;
     p3.l2_keep_b = 0;  // X is reused by every wave; the W tile is shared within one
@@ -595,6 +625,10 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
     p4.k_list = sk.list;
     p4.k_count = sk.count;
     p4.k_per_entry = tile_rows(pair) / BK;
+    if (filt) {
+      p4.fmask = mask_w;
+      p4.fmask_ld = pl.mask_w_ld;
+    }
     p4.l2_keep_b = 1;  // X again; the dZ column block is shared within one wave
     p4.l2_keep_frac = l2_keep_fraction((double)N * H * 2);
     p4.err_word = c.err_word;
@@ -615,6 +649,10 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
     p5.reduce_add = ci > 0 ? 1 : 0;
     p5.row_list = sk.list;
     p5.row_count = sk.count;
+    if (filt) {
+      p5.fmask = mask_x;
+      p5.fmask_ld = pl.mask_x_ld;
+    }
     p5.l2_keep_b = 1;  // the W chunk; the dZ row block is shared within one wave
     p5.l2_keep_frac = l2_keep_fraction((double)w * H * 2);
     p5.err_word = c.err_word;
@@ -639,7 +677,7 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
 // ===========================================================================
 extern "C" {
 
-int flce_abi_version(void) { return 102; }
+int flce_abi_version(void) { return 103; }
 
 const char* flce_status_string(flce_status s) {
   switch (s) {
@@ -730,6 +768,7 @@ void flce_options_init(flce_options* opt) {
   opt->reduction = FLCE_MEAN;
   opt->row_loss = nullptr;
   opt->skip_ignored_blocks = 0;
+  opt->grad_filter = 0.f;
 }
 
 }  // extern "C"
@@ -754,6 +793,7 @@ Common make_common(const void* X, const void* W, const int64_t* labels, int64_t 
                 o->z_loss,
                 o->row_loss,
                 o->skip_ignored_blocks,
+                o->grad_filter,
                 dtype,
                 o->reduction,
                 ws,

@@ -59,6 +59,8 @@ constexpr int STAGING_BUF_BYTES = 32 * 128;               // 32 rows x 128 bytes
 constexpr int STAGING_BYTES = NUM_EPI_WARPS * 2 * STAGING_BUF_BYTES;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int BARRIER_BYTES = 256;
+constexpr int STAGES_META = 8;          // >= STAGES of any instantiation
+constexpr int FILTER_MAX_KB = 1024;     // k-blocks of one filtered tile (keep bytes in smem)
 constexpr float LOG2E = 1.4426950408889634f;
 
 // Tile geometry of the two variants.
@@ -107,6 +109,20 @@ struct GemmParams {
   const int* k_list;
   const int* k_count;
   int k_per_entry;
+  // Gradient filtering (CCE-style).  The kDz launch marks, for every
+  // 32-token x 64-column block of dZ that holds a probability >= filter_thr
+  // or a target, maskX[token tile][vocab k-block] and maskW[vocab tile][token
+  // k-block] (tiles of mask_tile rows; the masks start zeroed).  A kStore
+  // launch given `fmask` (its own mask, row stride fmask_ld) walks only the
+  // k-blocks marked for its tile; the first k-block of a tile always runs.
+  uint8_t* mask_x_out;
+  uint8_t* mask_w_out;
+  int mask_x_ld;      // vocabulary k-blocks per token tile
+  int mask_w_ld;      // token k-blocks per vocabulary tile
+  int mask_tile;      // rows of the dX / dW tiles the masks describe
+  float filter_thr;
+  const uint8_t* fmask;
+  int fmask_ld;
   // L2 residency: the operand reused across waves of tiles (0 = A, 1 = B) is
   // loaded with an evict_last policy covering `l2_keep_frac` of its lines.
   int l2_keep_b;
@@ -119,7 +135,7 @@ struct GemmParams {
 template <Epi EPI, int STAGES, bool PAIR>
 constexpr int gemm_smem_bytes() {
   return STAGES * TileCfg<PAIR>::STAGE + (EPI == Epi::kLse ? 0 : STAGING_BYTES) + BARRIER_BYTES +
-         1024;
+         (EPI == Epi::kStore ? FILTER_MAX_KB : 0) + 1024;
 }
 
 // Row-block count and unit count of this launch (after skipping, if any).
@@ -158,6 +174,28 @@ __device__ __forceinline__ int kblock_count(const GemmParams& p, int num_kb) {
 __device__ __forceinline__ int kblock_at(const GemmParams& p, int i) {
   return p.k_list ? p.k_list[i / p.k_per_entry] * p.k_per_entry + i % p.k_per_entry : i;
 }
+
+// Gradient filtering: copy the keep bytes of row block mb's tile into shared
+// memory, indexed like the k loop (i-th walked k-block), and return the index
+// of the last kept one.  The first walked k-block always runs.
+__device__ __forceinline__ int load_tile_keep(const GemmParams& p, int mb, int num_kb,
+                                              uint8_t* keep) {
+  const uint8_t* row = p.fmask + (size_t)mb * p.fmask_ld;
+  if (!p.k_list) {
+    const uint4* src = reinterpret_cast<const uint4*>(row);
+    const int n16 = (num_kb + 15) / 16;
+#pragma unroll 4
+    for (int i = 0; i < n16; ++i) reinterpret_cast<uint4*>(keep)[i] = __ldg(src + i);
+  } else {
+#pragma unroll 4
+    for (int i = 0; i < num_kb; ++i) keep[i] = __ldg(row + kblock_at(p, i));
+  }
+  keep[0] = 1;
+  int last = num_kb - 1;
+  while (last > 0 && !keep[last]) --last;
+  return last;
+}
+
 
 // tcgen05.wait::ld with the loaded registers as operands, so no use of them
 // can be scheduled before the wait.
@@ -210,6 +248,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
   uint64_t* mma_done = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  int* stage_meta = abort_flag + 1;  // filtered launches: k-block index | last-of-tile flag
+  uint8_t* tile_keep = reinterpret_cast<uint8_t*>(stage_meta + STAGES_META);  // FILTER_MAX_KB
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -271,14 +311,19 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
         const int a_row = mb * Cfg::TILE_M + (int)rank * BM;
         for (int nb = nb0; nb < nb1 && ok; ++nb) {
           const int b_row = nb * BN + (int)rank * Cfg::B_ROWS;
+          // filtered launches: the last kept k-block of the tile ends it
+          const int last_kept = p.fmask ? load_tile_keep(p, mb, num_kb, tile_keep) : num_kb - 1;
           for (int ki = 0; ki < num_kb; ++ki) {
             const int kb = kblock_at(p, ki);
+            if (p.fmask && ki > last_kept) break;
+            if (p.fmask && !tile_keep[ki]) continue;
             const int s = it % STAGES;
             const uint32_t r = it / STAGES;
             if (!mbar_wait(&empty[s], (r & 1u) ^ 1u, ctx)) {
               ok = false;
               break;
             }
+            if (p.fmask && rank == 0) stage_meta[s] = kb | (ki == last_kept ? (1 << 30) : 0);
             uint8_t* a_dst = stages + s * Cfg::STAGE;
             uint8_t* b_dst = a_dst + Cfg::A_STAGE;
             if constexpr (PAIR) {
@@ -369,6 +414,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
               break;
             }
             tc_fence_after();
+            // filtered launches: the producer tells which stage ends the tile
+            const bool last_stage = p.fmask && (stage_meta[s] & (1 << 30));
             const uint32_t a_addr = smem_u32(stages + s * Cfg::STAGE);
             const uint32_t b_addr = a_addr + Cfg::A_STAGE;
 #pragma unroll
@@ -387,6 +434,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
             else
               mma_commit(&empty[s]);
             ++it;
+            if (last_stage) break;
           }
           if (!ok) break;
           if constexpr (PAIR)
@@ -498,16 +546,29 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
             tmem_ld_wait_regs(r1);
             uint32_t w[32];
             const long long off = lab_rel - c0;
+            float pmax = 0.f;
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
               const float za = __uint_as_float(r0[j]);
               const float zb = __uint_as_float(r1[j]);
-              float da = fmaf(dz_pcoef, ex2_approx(fmaf(za, LOG2E, dz_neg_lse2)), -dz_eps);
-              float db = fmaf(dz_pcoef, ex2_approx(fmaf(zb, LOG2E, dz_neg_lse2)), -dz_eps);
+              const float pa = ex2_approx(fmaf(za, LOG2E, dz_neg_lse2));
+              const float pb = ex2_approx(fmaf(zb, LOG2E, dz_neg_lse2));
+              pmax = fmaxf(pmax, fmaxf(pa, pb));
+              float da = fmaf(dz_pcoef, pa, -dz_eps);
+              float db = fmaf(dz_pcoef, pb, -dz_eps);
               if (off == j) da -= dz_tgt;
               if (off == j + 32) db -= dz_tgt;
               r0[j] = __float_as_uint(da);
               r1[j] = __float_as_uint(db);
+            }
+            if (p.mask_x_out) {
+              // this 32-token x 64-column block is kept if a valid row has a
+              // probability >= the threshold or its target in it
+              const bool keep_row = valid && (pmax >= p.filter_thr || (off >= 0 && off < 64));
+              if (__ballot_sync(0xffffffffu, keep_row) != 0u && lane == 0) {
+                p.mask_x_out[(size_t)(store_row0 / p.mask_tile) * p.mask_x_ld + c0 / 64] = 1;
+                p.mask_w_out[(size_t)(c0 / p.mask_tile) * p.mask_w_ld + store_row0 / 64] = 1;
+              }
             }
 #pragma unroll
             for (int j = 0; j < 16; ++j) {

@@ -23,6 +23,9 @@ positions, 4 Zipf rank-to-token permutation, 5 scaled W rows):
     seeded permutation of [0, V).
   * ignore positions: the first ``n_ignore`` entries of a seeded permutation
     of [0, N) get the label ``ignore_index``.
+  * peaked logits (``x_align`` > 0): after the labels are drawn, each valid row
+    x_i gets x_align * u_{y_i} added before rounding, u_j = W_j scaled to unit
+    RMS, so the target's logit stands out as it does for a trained model.
   * instruction-tuning masks (``labels="sft"``): N tokens are sequences of
     ``seq_len``; sequence b ignores its first floor(u_b * seq_len) tokens (the
     prompt), u_b uniform in ``prompt_frac``, drawn from stream k = 6; the other
@@ -62,6 +65,7 @@ class WorkloadSpec:
     ignore_index: int = IGNORE_INDEX
     reduction: str = "mean"
     seq_len: int = 0                       # "sft" labels: tokens per sequence
+    x_align: float = 0.0                   # pull each x_i towards its target's W row
     prompt_frac: tuple = (0.2, 0.8)        # "sft" labels: masked prompt share per sequence
 
     @property
@@ -83,13 +87,18 @@ GEMMA = WorkloadSpec("gemma2_n32768", N=32768, H=2304, V=256000, dtype="bf16",
                      labels="zipf", n_ignore=int(0.05 * 32768),
                      n_scaled_w_rows=2560, w_row_scale=8.0)
 
+# Peaked logits on the Llama-3 shape (target logit ~ 15 above the rest's
+# spread): the regime where gradient filtering drops most of dZ.
+LLAMA_PEAKED = WorkloadSpec("llama3_peaked_n8192", N=8192, H=4096, V=128256, dtype="bf16",
+                            n_ignore=round(0.05 * 8192), x_align=0.18)
+
 # Instruction tuning on the Llama-3 shape: 4 sequences of 4096 tokens whose
 # prompts (20-80% of each sequence) are masked ("Chunked and Fused
 # Cross-Entropy ...", "Numerical Considerations ...", item 2).
 LLAMA_SFT = WorkloadSpec("llama3_sft_n16384", N=16384, H=4096, V=128256, dtype="bf16",
                          labels="sft", seq_len=4096)
 
-CONFIGS = {s.name: s for s in (TINY, LLAMA, LLAMA_LONG, QWEN, GEMMA, LLAMA_SFT)}
+CONFIGS = {s.name: s for s in (TINY, LLAMA, LLAMA_LONG, QWEN, GEMMA, LLAMA_SFT, LLAMA_PEAKED)}
 
 
 def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
@@ -222,13 +231,24 @@ def make_workload(spec: WorkloadSpec | str, seed: int = 0) -> Workload:
     bf16 = spec.dtype == "bf16"
     if spec.dtype not in ("bf16", "fp32"):
         raise ValueError(f"unknown dtype {spec.dtype!r}")
-    x = _normal_matrix(seed, 0, spec.N, spec.H, spec.x_std, spec.x_rms_rows, bf16)
+    x = _normal_matrix(seed, 0, spec.N, spec.H, spec.x_std, spec.x_rms_rows,
+                       bf16 and not spec.x_align)
     scaled = None
     if spec.n_scaled_w_rows:
         scaled = _rng(seed, 5).permutation(spec.V)[:spec.n_scaled_w_rows]
     w = _normal_matrix(seed, 1, spec.V, spec.H, spec.w_std, False, bf16,
                        scale_rows=scaled, row_scale=spec.w_row_scale)
     labels = make_labels(spec, seed)
+    if spec.x_align:
+        wf = bf16_bits_to_f32(w) if bf16 else w
+        rows = np.flatnonzero(labels != spec.ignore_index)
+        for r0 in range(0, len(rows), 4096):
+            rr = rows[r0:r0 + 4096]
+            u = wf[labels[rr]].astype(np.float32)
+            u /= np.sqrt(np.mean(u.astype(np.float64) ** 2, axis=1)).astype(np.float32)[:, None]
+            x[rr] += np.float32(spec.x_align) * u
+        if bf16:
+            x = f32_to_bf16_bits(x)
     return Workload(spec, seed, x, w, labels)
 
 

@@ -75,3 +75,14 @@ def test_sft_prompt_spans():
         # a contiguous prefix of 30-60% of the sequence is masked
         assert len(ign) == ign[-1] + 1 and 75 <= len(ign) <= 150
         assert np.all(seq[len(ign):] >= 0)
+
+
+def test_peaked_targets_stand_out():
+    spec = I.custom_spec("p", N=200, H=256, V=3000, dtype="bf16", x_align=3.0, n_ignore=10)
+    wl = I.make_workload(spec, 0)
+    x = wl.x_f32().astype(np.float64)
+    w = wl.w_f32().astype(np.float64)
+    z = x @ w.T
+    valid = wl.labels != I.IGNORE_INDEX
+    zy = z[np.flatnonzero(valid), wl.labels[valid]]
+    assert np.median(zy) > 10.0 and np.std(z) < 2.0

@@ -36,7 +36,7 @@ def test_header_exports_all(L):
 
 
 def test_status_strings_and_version(L):
-    assert L.flce_abi_version() == 102
+    assert L.flce_abi_version() == 103
     for s in range(7):
         assert L.flce_status_string(s).decode().startswith("FLCE_")
 
@@ -126,6 +126,7 @@ def test_options_struct_layout(L):
     L.flce_options_init(ctypes.byref(o))
     assert o.struct_size == ctypes.sizeof(B.FlceOptions)
     assert (o.ignore_index, o.smoothing, o.z_loss, o.reduction, o.row_loss) == (-100, 0.0, 0.0, 0, None)
+    assert (o.skip_ignored_blocks, o.grad_filter) == (0, 0.0)
     # a struct of another size is rejected before any CUDA call
     o.struct_size = 8
     P = ctypes.c_void_p
