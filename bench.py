@@ -50,6 +50,9 @@ def parse_args():
     ap.add_argument("--reference-rows", type=int, default=128,
                     help="token rows per oracle step of --impl reference")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--summarize-traffic", metavar="NCU_CSV", default=None,
+                    help="write profiles/traffic_<workload>.txt from an ncu --csv capture of "
+                         "dram__bytes_read.sum / dram__bytes_write.sum over one step, then exit")
     ap.add_argument("--l2-hints", action="store_true",
                     help="evict_last L2 policy for the operand re-read on every wave of tiles")
     ap.add_argument("--vocab-shards", type=int, default=0,
@@ -64,6 +67,78 @@ def parse_args():
     ap.add_argument("--single-cta", action="store_true",
                     help="128x256 single-CTA tiles instead of 256x256 CTA-pair tiles")
     return ap.parse_args()
+
+
+KERNEL_SOURCES = ("gemm_core.cuh", "ptx.cuh", "aux_kernels.cuh", "flce_api.cu")
+KIND_BY_EPI = {("0", None): "fwd_logits_lse", ("1", None): "bwd_dz_recompute",
+               ("2", "1"): "bwd_dw_gemm", ("2", "0"): "bwd_dx_gemm"}
+
+
+def kernel_source_hash() -> str:
+    """SHA-256 of the CUDA sources the GEMM kinds are built from."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "linear_cross_entropy_logit_gb300", "csrc", name), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def traffic_path(workload: str) -> str:
+    return os.path.join(ROOT, "profiles", f"traffic_{workload}.txt")
+
+
+def summarize_traffic(csv_path: str, workload: str) -> None:
+    """Per-kind DRAM bytes per launch from an ncu CSV (mangled kernel names)."""
+    import csv
+    import re
+    per = {}
+    with open(csv_path) as fh:
+        rows = list(csv.DictReader(l for l in fh if not l.startswith("==")))
+    for r in rows:
+        name = r["Kernel Name"]
+        m = (re.search(r"EpiE(\d)ELb(\d)ELb(\d)", name)
+             or re.search(r"gemm_(?:pair_)?kernel<(\d), (\d), (\d), \d+(?:, \d)?>", name))
+        if not m:
+            continue
+        kind = KIND_BY_EPI.get((m.group(1), None)) or KIND_BY_EPI[(m.group(1), m.group(2))]
+        d = per.setdefault(kind, {"ids": set(), "read": 0.0, "write": 0.0})
+        d["ids"].add(r["ID"])
+        scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}.get(r["Metric Unit"], None)
+        if scale is None:
+            continue
+        v = float(r["Metric Value"].replace(",", "")) * scale
+        if r["Metric Name"] == "dram__bytes_read.sum":
+            d["read"] += v
+        elif r["Metric Name"] == "dram__bytes_write.sum":
+            d["write"] += v
+    lines = [f"# DRAM bytes per launch, {workload}, from {os.path.basename(csv_path)}",
+             f"# source_sha256 {kernel_source_hash()}",
+             "# kind launches read_bytes_per_launch write_bytes_per_launch"]
+    for kind, d in sorted(per.items()):
+        n = len(d["ids"])
+        lines.append(f"{kind} {n} {d['read'] / n:.0f} {d['write'] / n:.0f}")
+    with open(traffic_path(workload), "w") as fh:
+        fh.write("\n".join(lines) + "\n")
+    print("\n".join(lines))
+
+
+def load_traffic(workload: str):
+    """{kind: bytes per launch} if the capture matches the current kernel source."""
+    try:
+        with open(traffic_path(workload)) as fh:
+            lines = fh.read().splitlines()
+    except OSError:
+        return None
+    sha = next((l.split()[2] for l in lines if l.startswith("# source_sha256")), None)
+    if sha != kernel_source_hash():
+        return None
+    out = {}
+    for l in lines:
+        if l and not l.startswith("#"):
+            kind, n, rd, wr = l.split()
+            out[kind] = float(rd) + float(wr)
+    return out
 
 
 def host_cores() -> int:
@@ -441,10 +516,14 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                        "tflops": flops_kind * args.steps / (kms / 1e3) / 1e12}
     dom = max(kinds, key=lambda k: kinds[k]["ms_total"]) if kinds else None
     roofline = None
+    dense_default = not (args.skip_ignored or args.grad_filter or args.vocab_shards > 1 or
+                         args.shape or args.single_cta or args.l2_hints)
+    traffic = load_traffic(spec.name) if dense_default else None
     if dom:
         ach = kinds[dom]["tflops"]
         roofline = {"bound": "tensor", "achieved": ach, "peak": pk["bf16_sustained"],
-                    "unit": "TFLOP/s", "frac": ach / pk["bf16_sustained"], "traffic": None,
+                    "unit": "TFLOP/s", "frac": ach / pk["bf16_sustained"],
+                    "traffic": traffic.get(dom) if traffic else None,
                     "kernel": dom,
                     "peak_source": f"{pk['source']} bf16 sustained (MEASURED_PEAKS.json)"
                     if pk["source"] == "measured" else "fallback bf16 sustained"}
@@ -495,6 +574,9 @@ def run_ours(args, rank: int, world: int, local_rank: int):
 
 def main():
     args = parse_args()
+    if args.summarize_traffic:
+        summarize_traffic(args.summarize_traffic, args.workload)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

@@ -276,18 +276,18 @@ flce_status map_f32_out(CUtensorMap* m, const void* base, uint64_t cols, uint64_
                   32);
 }
 
-template <Epi EPI, bool A_MN, bool B_MN, bool PAIR>
+template <Epi EPI, bool A_MN, bool B_MN, bool PAIR, bool EXT>
 flce_status launch_gemm(int dev, int num_sms, const CUtensorMap& a, const CUtensorMap& b,
                         const CUtensorMap& out, const GemmParams& p, cudaStream_t st,
                         int prof_kind = -1) {
   constexpr int stages = PAIR ? kPairStages : kStages;
   auto kern = [] {
     if constexpr (PAIR)
-      return gemm_pair_kernel<EPI, A_MN, B_MN, stages>;
+      return gemm_pair_kernel<EPI, A_MN, B_MN, stages, EXT>;
     else
-      return gemm_kernel<EPI, A_MN, B_MN, stages>;
+      return gemm_kernel<EPI, A_MN, B_MN, stages, EXT>;
   }();
-  constexpr int smem = gemm_smem_bytes<EPI, stages, PAIR>();
+  constexpr int smem = gemm_smem_bytes<EPI, stages, PAIR, EXT>();
   static std::once_flag flags[kMaxDevices];
   cudaError_t attr_err = cudaSuccess;
   std::call_once(flags[dev], [&] {
@@ -330,11 +330,14 @@ flce_status launch_gemm(int dev, int num_sms, const CUtensorMap& a, const CUtens
 
 // Run-time choice between the 1-CTA (128 x 256) and CTA-pair (256 x 256) kernels.
 template <Epi EPI, bool A_MN, bool B_MN>
-flce_status launch_tile(bool pair, int dev, int num_sms, const CUtensorMap& a,
+flce_status launch_tile(bool pair, bool ext, int dev, int num_sms, const CUtensorMap& a,
                         const CUtensorMap& b, const CUtensorMap& out, const GemmParams& p,
                         cudaStream_t st, int prof_kind = -1) {
-  return pair ? launch_gemm<EPI, A_MN, B_MN, true>(dev, num_sms, a, b, out, p, st, prof_kind)
-              : launch_gemm<EPI, A_MN, B_MN, false>(dev, num_sms, a, b, out, p, st, prof_kind);
+  if (ext)
+    return pair ? launch_gemm<EPI, A_MN, B_MN, true, true>(dev, num_sms, a, b, out, p, st, prof_kind)
+                : launch_gemm<EPI, A_MN, B_MN, false, true>(dev, num_sms, a, b, out, p, st, prof_kind);
+  return pair ? launch_gemm<EPI, A_MN, B_MN, true, false>(dev, num_sms, a, b, out, p, st, prof_kind)
+              : launch_gemm<EPI, A_MN, B_MN, false, false>(dev, num_sms, a, b, out, p, st, prof_kind);
 }
 
 bool use_pair() { return g_cta_pair.load() != 0; }
@@ -399,6 +402,11 @@ flce_status validate_common(const Common& c, int mode, Plan* pl) {
   if (!c.ws || !aligned(c.ws, kAlign)) return FLCE_ERR_WORKSPACE;
   if (c.ws_bytes < pl->total) return FLCE_ERR_WORKSPACE;
   return FLCE_OK;
+}
+
+// Whether a call needs the kernels' optional features compiled in.
+bool ext_features(const Common& c) {
+  return c.skip_ignored || c.grad_filter > 0.f || g_l2_hints.load() != 0;
 }
 
 // Skip lists for SFT-style masking: token blocks of `tile_rows(pair)` rows with
@@ -491,7 +499,8 @@ flce_status run_forward(const Common& c, const Plan& pl, int dev, int sms, const
     p.row_count = sk.count;
     p.err_word = c.err_word;
     p.timeout_ns = kTimeoutNs;
-    FLCE_TRY((launch_tile<Epi::kLse, false, false>(pair, dev, sms, tmX, tmW, tmX, p, c.st, 0)));
+    FLCE_TRY((launch_tile<Epi::kLse, false, false>(pair, ext_features(c), dev, sms, tmX, tmW, tmX, p,
+                                                  c.st, 0)));
     if (shard_out) {
       // vocabulary shard: one merged partial per row, no loss yet
       shard_partial_kernel<<<pl.merge_blocks, MERGE_THREADS, 0, c.st>>>(
@@ -540,6 +549,7 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
   FLCE_TRY(map_f32_out(&tmDxAcc, dx_acc, H, N, H));
 
   const bool pair = use_pair();
+  const bool ext = ext_features(c);
   const int m_blocks_tok = (int)ceil_div(N, tile_rows(pair));
   SkipLists sk;
   FLCE_TRY(build_skip_lists(c, pl, pair, &sk));
@@ -608,7 +618,8 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
     p3.l2_keep_frac = l2_keep_fraction((double)N * H * 2);
     p3.err_word = c.err_word;
     p3.timeout_ns = kTimeoutNs;
-    FLCE_TRY((launch_tile<Epi::kDz, false, false>(pair, dev, sms, tmX_k, tmWc_k, tmDzSt, p3, c.st, 1)));
+    FLCE_TRY((launch_tile<Epi::kDz, false, false>(pair, ext, dev, sms, tmX_k, tmWc_k, tmDzSt, p3,
+                                                  c.st, 1)));
 
     // K4: dW[v0:v0+w, :] = dZ_chunk^T X   (K = N tokens)
     GemmParams p4{};
@@ -633,7 +644,8 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
     p4.l2_keep_frac = l2_keep_fraction((double)N * H * 2);
     p4.err_word = c.err_word;
     p4.timeout_ns = kTimeoutNs;
-    FLCE_TRY((launch_tile<Epi::kStore, true, true>(pair, dev, sms, tmDz_mn, tmX_mn, tmDw, p4, c.st, 2)));
+    FLCE_TRY((launch_tile<Epi::kStore, true, true>(pair, ext, dev, sms, tmDz_mn, tmX_mn, tmDw, p4,
+                                                   c.st, 2)));
 
     // K5: dX_acc (+)= dZ_chunk W[v0:v0+w, :]   (K = w vocabulary columns)
     GemmParams p5{};
@@ -657,7 +669,8 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
     p5.l2_keep_frac = l2_keep_fraction((double)w * H * 2);
     p5.err_word = c.err_word;
     p5.timeout_ns = kTimeoutNs;
-    FLCE_TRY((launch_tile<Epi::kStore, false, true>(pair, dev, sms, tmDz_k, tmWc_mn, tmDxAcc, p5, c.st, 3)));
+    FLCE_TRY((launch_tile<Epi::kStore, false, true>(pair, ext, dev, sms, tmDz_k, tmWc_mn, tmDxAcc,
+                                                    p5, c.st, 3)));
   }
   if (c.dtype == FLCE_BF16 && !c.dx_partial_f32) {
     const size_t n4 = (size_t)N * H / 4;
@@ -1077,10 +1090,10 @@ flce_status flce_debug_gemm(const void* A, const void* B, float* D, int64_t M, i
   p.reduce_add = accumulate ? 1 : 0;
   p.err_word = err_word;
   p.timeout_ns = kTimeoutNs;
-  if (!a_mn && !b_mn) return launch_tile<Epi::kStore, false, false>(pair, dev, sms, ta, tb, td, p, st);
-  if (!a_mn && b_mn) return launch_tile<Epi::kStore, false, true>(pair, dev, sms, ta, tb, td, p, st);
-  if (a_mn && !b_mn) return launch_tile<Epi::kStore, true, false>(pair, dev, sms, ta, tb, td, p, st);
-  return launch_tile<Epi::kStore, true, true>(pair, dev, sms, ta, tb, td, p, st);
+  if (!a_mn && !b_mn) return launch_tile<Epi::kStore, false, false>(pair, false, dev, sms, ta, tb, td, p, st);
+  if (!a_mn && b_mn) return launch_tile<Epi::kStore, false, true>(pair, false, dev, sms, ta, tb, td, p, st);
+  if (a_mn && !b_mn) return launch_tile<Epi::kStore, true, false>(pair, false, dev, sms, ta, tb, td, p, st);
+  return launch_tile<Epi::kStore, true, true>(pair, false, dev, sms, ta, tb, td, p, st);
 }
 
 }  // extern "C"

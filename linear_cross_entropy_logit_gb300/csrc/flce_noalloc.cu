@@ -118,7 +118,7 @@ flce_status na_setup(int* scratch_sms, void** scratch_out) {
   if (!g_na_attr[dev]) {
     e = cudaFuncSetAttribute(gemm_kernel<Epi::kLse, false, false, kNaStages>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             gemm_smem_bytes<Epi::kLse, kNaStages, false>());
+                             gemm_smem_bytes<Epi::kLse, kNaStages, false, false>());
     if (e != cudaSuccess) return na_cuda_fail(e, "cudaFuncSetAttribute");
     g_na_attr[dev] = true;
   }
@@ -219,7 +219,7 @@ extern "C" flce_status flce_forward_noalloc(const void* X, const void* W, const 
     p.timeout_ns = kNaTimeoutNs;
     const int grid = std::min(p.num_units, sms);
     gemm_kernel<Epi::kLse, false, false, kNaStages>
-        <<<grid, NUM_THREADS, gemm_smem_bytes<Epi::kLse, kNaStages, false>(), st>>>(tmX, tmW, tmX, p);
+        <<<grid, NUM_THREADS, gemm_smem_bytes<Epi::kLse, kNaStages, false, false>(), st>>>(tmX, tmW, tmX, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return na_cuda_fail(e, "forward GEMM launch");
     lse_merge_kernel<<<pl.merge_blocks, MERGE_THREADS, 0, st>>>(
         p.partials, pl.n_groups, pl.m_pad, (int)N, (int)V, labels, ignore_index, smoothing, 0.f,

@@ -132,10 +132,13 @@ struct GemmParams {
   unsigned long long timeout_ns;
 };
 
-template <Epi EPI, int STAGES, bool PAIR>
+// EXT = the optional features (token-block skip lists, gradient filtering,
+// L2 hints) are compiled in.  Calls that use none of them run EXT = false,
+// whose loops carry no trace of them.
+template <Epi EPI, int STAGES, bool PAIR, bool EXT>
 constexpr int gemm_smem_bytes() {
   return STAGES * TileCfg<PAIR>::STAGE + (EPI == Epi::kLse ? 0 : STAGING_BYTES) + BARRIER_BYTES +
-         (EPI == Epi::kStore ? FILTER_MAX_KB : 0) + 1024;
+         ((EXT && EPI == Epi::kStore) ? FILTER_MAX_KB : 0) + 1024;
 }
 
 // Row-block count and unit count of this launch (after skipping, if any).
@@ -152,6 +155,7 @@ __device__ __forceinline__ UnitSpace unit_space(const GemmParams& p) {
   return {p.m_blocks, p.num_units};
 }
 
+template <bool EXT>
 __device__ __forceinline__ void unit_coords(const GemmParams& p, const UnitSpace& us, int u,
                                             int& mb, int& nb0, int& nb1, int& g) {
   if (p.m_fastest) {
@@ -161,7 +165,9 @@ __device__ __forceinline__ void unit_coords(const GemmParams& p, const UnitSpace
     g = u % p.n_groups;
     mb = u / p.n_groups;
   }
-  if (p.row_list) mb = p.row_list[mb];
+  if constexpr (EXT) {
+    if (p.row_list) mb = p.row_list[mb];
+  }
   nb0 = g * p.group_len;
   nb1 = min(nb0 + p.group_len, p.n_blocks);
 }
@@ -231,7 +237,7 @@ __device__ __forceinline__ void staging_write_row(uint32_t buf, int row, const u
   }
 }
 
-template <Epi EPI, bool A_MN, bool B_MN, int STAGES, bool PAIR>
+template <Epi EPI, bool A_MN, bool B_MN, int STAGES, bool PAIR, bool EXT>
 __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensorMap& tmB,
                                           const CUtensorMap& tmOut, const GemmParams& p) {
   using Cfg = TileCfg<PAIR>;
@@ -294,36 +300,48 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
   const uint32_t tmem_base = *tmem_slot;
   const WaitCtx ctx{abort_flag, p.err_word, p.timeout_ns};
   const int num_kb_all = (p.k_size + BK - 1) / BK;
-  const int num_kb = kblock_count(p, num_kb_all);
-  const UnitSpace us = unit_space(p);
+  const int num_kb = EXT ? kblock_count(p, num_kb_all) : num_kb_all;
+  const UnitSpace us = EXT ? unit_space(p) : UnitSpace{p.m_blocks, p.num_units};
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
-      const uint64_t keep = l2_policy_evict_last(p.l2_keep_frac);
-      const bool keep_a = p.l2_keep_frac > 0.f && !p.l2_keep_b;
-      const bool keep_b = p.l2_keep_frac > 0.f && p.l2_keep_b;
+      uint64_t keep = 0;
+      bool keep_a = false, keep_b = false;
+      if constexpr (EXT) {
+        keep = l2_policy_evict_last(p.l2_keep_frac);
+        keep_a = p.l2_keep_frac > 0.f && !p.l2_keep_b;
+        keep_b = p.l2_keep_frac > 0.f && p.l2_keep_b;
+      }
       for (int u = pair_id; u < us.num_units && ok; u += num_pairs) {
         int mb, nb0, nb1, g;
-        unit_coords(p, us, u, mb, nb0, nb1, g);
+        unit_coords<EXT>(p, us, u, mb, nb0, nb1, g);
         const int a_row = mb * Cfg::TILE_M + (int)rank * BM;
         for (int nb = nb0; nb < nb1 && ok; ++nb) {
           const int b_row = nb * BN + (int)rank * Cfg::B_ROWS;
           // filtered launches: the last kept k-block of the tile ends it
-          const int last_kept = p.fmask ? load_tile_keep(p, mb, num_kb, tile_keep) : num_kb - 1;
+          int last_kept = num_kb - 1;
+          if constexpr (EXT) {
+            if (p.fmask) last_kept = load_tile_keep(p, mb, num_kb, tile_keep);
+          }
           for (int ki = 0; ki < num_kb; ++ki) {
-            const int kb = kblock_at(p, ki);
-            if (p.fmask && ki > last_kept) break;
-            if (p.fmask && !tile_keep[ki]) continue;
+            int kb = ki;
+            if constexpr (EXT) {
+              kb = kblock_at(p, ki);
+              if (p.fmask && ki > last_kept) break;
+              if (p.fmask && !tile_keep[ki]) continue;
+            }
             const int s = it % STAGES;
             const uint32_t r = it / STAGES;
             if (!mbar_wait(&empty[s], (r & 1u) ^ 1u, ctx)) {
               ok = false;
               break;
             }
-            if (p.fmask && rank == 0) stage_meta[s] = kb | (ki == last_kept ? (1 << 30) : 0);
+            if constexpr (EXT) {
+              if (p.fmask && rank == 0) stage_meta[s] = kb | (ki == last_kept ? (1 << 30) : 0);
+            }
             uint8_t* a_dst = stages + s * Cfg::STAGE;
             uint8_t* b_dst = a_dst + Cfg::A_STAGE;
             if constexpr (PAIR) {
@@ -331,47 +349,83 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
               // only the leader arms with the pair's byte count.
               const uint32_t bar = mapa_shared(smem_u32(&full[s]), 0);
               if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * Cfg::STAGE);
-              auto ld = [&](void* dst, const CUtensorMap* m, int x, int y, bool hint) {
-                if (hint)
-                  tma_load_2d_pair_hint(dst, m, bar, x, y, keep);
-                else
-                  tma_load_2d_pair(dst, m, bar, x, y);
-              };
-              if constexpr (!A_MN) {
-                ld(a_dst, &tmA, kb * BK, a_row, keep_a);
-              } else {
+              if constexpr (!EXT) {
+                if constexpr (!A_MN) {
+                  tma_load_2d_pair(a_dst, &tmA, bar, kb * BK, a_row);
+                } else {
 #pragma unroll
-                for (int i = 0; i < BM / 64; ++i)
-                  ld(a_dst + i * MN_BOX_BYTES, &tmA, a_row + i * 64, kb * BK, keep_a);
-              }
-              if constexpr (!B_MN) {
-                ld(b_dst, &tmB, kb * BK, b_row, keep_b);
-              } else {
+                  for (int i = 0; i < BM / 64; ++i)
+                    tma_load_2d_pair(a_dst + i * MN_BOX_BYTES, &tmA, bar, a_row + i * 64, kb * BK);
+                }
+                if constexpr (!B_MN) {
+                  tma_load_2d_pair(b_dst, &tmB, bar, kb * BK, b_row);
+                } else {
 #pragma unroll
-                for (int i = 0; i < Cfg::B_ROWS / 64; ++i)
-                  ld(b_dst + i * MN_BOX_BYTES, &tmB, b_row + i * 64, kb * BK, keep_b);
+                  for (int i = 0; i < Cfg::B_ROWS / 64; ++i)
+                    tma_load_2d_pair(b_dst + i * MN_BOX_BYTES, &tmB, bar, b_row + i * 64,
+                                     kb * BK);
+                }
+              } else {
+                auto ld = [&](void* dst, const CUtensorMap* m, int x, int y, bool hint) {
+                  if (hint)
+                    tma_load_2d_pair_hint(dst, m, bar, x, y, keep);
+                  else
+                    tma_load_2d_pair(dst, m, bar, x, y);
+                };
+                if constexpr (!A_MN) {
+                  ld(a_dst, &tmA, kb * BK, a_row, keep_a);
+                } else {
+#pragma unroll
+                  for (int i = 0; i < BM / 64; ++i)
+                    ld(a_dst + i * MN_BOX_BYTES, &tmA, a_row + i * 64, kb * BK, keep_a);
+                }
+                if constexpr (!B_MN) {
+                  ld(b_dst, &tmB, kb * BK, b_row, keep_b);
+                } else {
+#pragma unroll
+                  for (int i = 0; i < Cfg::B_ROWS / 64; ++i)
+                    ld(b_dst + i * MN_BOX_BYTES, &tmB, b_row + i * 64, kb * BK, keep_b);
+                }
               }
             } else {
               mbar_arrive_expect_tx(&full[s], Cfg::STAGE);
-              auto ld = [&](void* dst, const CUtensorMap* m, int x, int y, bool hint) {
-                if (hint)
-                  tma_load_2d_hint(dst, m, &full[s], x, y, keep);
-                else
-                  tma_load_2d(dst, m, &full[s], x, y);
-              };
-              if constexpr (!A_MN) {
-                ld(a_dst, &tmA, kb * BK, a_row, keep_a);
-              } else {
+              if constexpr (!EXT) {
+                if constexpr (!A_MN) {
+                  tma_load_2d(a_dst, &tmA, &full[s], kb * BK, a_row);
+                } else {
 #pragma unroll
-                for (int i = 0; i < BM / 64; ++i)
-                  ld(a_dst + i * MN_BOX_BYTES, &tmA, a_row + i * 64, kb * BK, keep_a);
-              }
-              if constexpr (!B_MN) {
-                ld(b_dst, &tmB, kb * BK, b_row, keep_b);
-              } else {
+                  for (int i = 0; i < BM / 64; ++i)
+                    tma_load_2d(a_dst + i * MN_BOX_BYTES, &tmA, &full[s], a_row + i * 64, kb * BK);
+                }
+                if constexpr (!B_MN) {
+                  tma_load_2d(b_dst, &tmB, &full[s], kb * BK, b_row);
+                } else {
 #pragma unroll
-                for (int i = 0; i < Cfg::B_ROWS / 64; ++i)
-                  ld(b_dst + i * MN_BOX_BYTES, &tmB, b_row + i * 64, kb * BK, keep_b);
+                  for (int i = 0; i < Cfg::B_ROWS / 64; ++i)
+                    tma_load_2d(b_dst + i * MN_BOX_BYTES, &tmB, &full[s], b_row + i * 64,
+                                kb * BK);
+                }
+              } else {
+                auto ld = [&](void* dst, const CUtensorMap* m, int x, int y, bool hint) {
+                  if (hint)
+                    tma_load_2d_hint(dst, m, &full[s], x, y, keep);
+                  else
+                    tma_load_2d(dst, m, &full[s], x, y);
+                };
+                if constexpr (!A_MN) {
+                  ld(a_dst, &tmA, kb * BK, a_row, keep_a);
+                } else {
+#pragma unroll
+                  for (int i = 0; i < BM / 64; ++i)
+                    ld(a_dst + i * MN_BOX_BYTES, &tmA, a_row + i * 64, kb * BK, keep_a);
+                }
+                if constexpr (!B_MN) {
+                  ld(b_dst, &tmB, kb * BK, b_row, keep_b);
+                } else {
+#pragma unroll
+                  for (int i = 0; i < Cfg::B_ROWS / 64; ++i)
+                    ld(b_dst + i * MN_BOX_BYTES, &tmB, b_row + i * 64, kb * BK, keep_b);
+                }
               }
             }
             ++it;
@@ -396,7 +450,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
       bool ok = true;
       for (int u = pair_id; u < us.num_units && ok; u += num_pairs) {
         int mb, nb0, nb1, g;
-        unit_coords(p, us, u, mb, nb0, nb1, g);
+        unit_coords<EXT>(p, us, u, mb, nb0, nb1, g);
         for (int nb = nb0; nb < nb1 && ok; ++nb) {
           const uint32_t acc = tile & 1u;
           const uint32_t ra = tile >> 1;
@@ -415,7 +469,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
             }
             tc_fence_after();
             // filtered launches: the producer tells which stage ends the tile
-            const bool last_stage = p.fmask && (stage_meta[s] & (1 << 30));
+            bool last_stage = false;
+            if constexpr (EXT) last_stage = p.fmask && (stage_meta[s] & (1 << 30));
             const uint32_t a_addr = smem_u32(stages + s * Cfg::STAGE);
             const uint32_t b_addr = a_addr + Cfg::A_STAGE;
 #pragma unroll
@@ -464,7 +519,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
 
     for (int u = pair_id; u < us.num_units && ok; u += num_pairs) {
       int mb, nb0, nb1, g;
-      unit_coords(p, us, u, mb, nb0, nb1, g);
+      unit_coords<EXT>(p, us, u, mb, nb0, nb1, g);
       const int row = mb * Cfg::TILE_M + row_in_tile;
       const int store_row0 = mb * Cfg::TILE_M + (int)rank * BM + q * 32;
       const bool row_ok = row < p.m_size;
@@ -553,7 +608,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
               const float zb = __uint_as_float(r1[j]);
               const float pa = ex2_approx(fmaf(za, LOG2E, dz_neg_lse2));
               const float pb = ex2_approx(fmaf(zb, LOG2E, dz_neg_lse2));
-              pmax = fmaxf(pmax, fmaxf(pa, pb));
+              if constexpr (EXT) pmax = fmaxf(pmax, fmaxf(pa, pb));
               float da = fmaf(dz_pcoef, pa, -dz_eps);
               float db = fmaf(dz_pcoef, pb, -dz_eps);
               if (off == j) da -= dz_tgt;
@@ -561,7 +616,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
               r0[j] = __float_as_uint(da);
               r1[j] = __float_as_uint(db);
             }
-            if (p.mask_x_out) {
+            if (EXT && p.mask_x_out) {
               // this 32-token x 64-column block is kept if a valid row has a
               // probability >= the threshold or its target in it
               const bool keep_row = valid && (pmax >= p.filter_thr || (off >= 0 && off < 64));
@@ -594,7 +649,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
             uint32_t r[32];
             tmem_ld_32x32b_x32(taddr + sl * 32, r);
             tmem_ld_wait_regs(r);
-            if (num_kb == 0) {  // every token block skipped: the product is zero
+            if (EXT && num_kb == 0) {  // every token block skipped: the product is zero
 #pragma unroll
               for (int j = 0; j < 32; ++j) r[j] = 0u;
             }
@@ -660,19 +715,19 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
   }
 }
 
-template <Epi EPI, bool A_MN, bool B_MN, int STAGES>
+template <Epi EPI, bool A_MN, bool B_MN, int STAGES, bool EXT = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmOut, const GemmParams p) {
-  gemm_body<EPI, A_MN, B_MN, STAGES, false>(tmA, tmB, tmOut, p);
+  gemm_body<EPI, A_MN, B_MN, STAGES, false, EXT>(tmA, tmB, tmOut, p);
 }
 
-template <Epi EPI, bool A_MN, bool B_MN, int STAGES>
+template <Epi EPI, bool A_MN, bool B_MN, int STAGES, bool EXT = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmOut, const GemmParams p) {
-  gemm_body<EPI, A_MN, B_MN, STAGES, true>(tmA, tmB, tmOut, p);
+  gemm_body<EPI, A_MN, B_MN, STAGES, true, EXT>(tmA, tmB, tmOut, p);
 }
 
 }  // namespace flce
