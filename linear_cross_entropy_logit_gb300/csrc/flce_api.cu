@@ -18,6 +18,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cmath>
 #include <atomic>
 #include <cstdio>
 #include <cstring>
@@ -342,6 +343,20 @@ flce_status launch_tile(bool pair, bool ext, int dev, int num_sms, const CUtenso
 
 bool use_pair() { return g_cta_pair.load() != 0; }
 
+// Row-block bands for the launches that re-read X (forward, dZ recompute):
+// with all row blocks in flight, X (N x H bf16) competes in L2 with the
+// streamed W tiles and is re-read from DRAM several times.  Splitting the row
+// blocks into ceil(X / 40 MiB) bands (at most 4) walked one after another costs
+// one more pass over W per band but keeps each band's X resident; measured on
+// a GB300 it cut the dZ launch's DRAM reads from ~1.0 to 0.42 GB at the
+// Llama-3 shape and sped the step up ~2% (Llama-3 and Gemma-2 shapes).
+int x_band(int64_t N, int64_t H, int m_blocks) {
+  const double x_bytes = (double)N * H * 2;
+  if (x_bytes <= 48.0 * (1 << 20)) return 0;
+  const int bands = (int)std::min(4.0, std::ceil(x_bytes / (40.0 * (1 << 20))));
+  return bands > 1 ? (m_blocks + bands - 1) / bands : 0;
+}
+
 // Fraction of the reused operand's lines kept in L2 with evict_last priority:
 // about 64 MB of the 129 MB L2 is given to it, the rest streams.
 std::atomic<int> g_l2_hints{0};
@@ -485,6 +500,7 @@ flce_status run_forward(const Common& c, const Plan& pl, int dev, int sms, const
     p.n_groups = pl.n_groups;
     p.num_units = p.m_blocks * pl.n_groups;
     p.m_fastest = 1;
+    p.m_band = x_band(c.N, c.H, p.m_blocks);
     p.labels = c.labels;
     p.ignore_index = c.ignore_index;
     p.vocab = (int)c.vocab_total;
@@ -595,6 +611,7 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
     p3.n_groups = p3.n_blocks;
     p3.num_units = p3.m_blocks * p3.n_groups;
     p3.m_fastest = 1;
+    p3.m_band = x_band(N, H, p3.m_blocks);
     p3.labels = c.labels;
     p3.ignore_index = c.ignore_index;
     p3.vocab = (int)c.vocab_total;

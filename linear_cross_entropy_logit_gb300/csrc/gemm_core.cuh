@@ -85,6 +85,7 @@ struct GemmParams {
   int n_groups;    // ceil(n_blocks / group_len)
   int num_units;   // m_blocks * n_groups
   int m_fastest;   // 1: consecutive units walk row blocks (share B); 0: walk column groups
+  int m_band;      // m_fastest: walk row blocks in bands of this many (0 = all at once)
   // kLse / kDz
   const int64_t* labels;  // per D row (token)
   long long ignore_index;
@@ -159,8 +160,19 @@ template <bool EXT>
 __device__ __forceinline__ void unit_coords(const GemmParams& p, const UnitSpace& us, int u,
                                             int& mb, int& nb0, int& nb1, int& g) {
   if (p.m_fastest) {
-    mb = u % us.m_blocks;
-    g = u / us.m_blocks;
+    if (p.m_band > 0 && p.m_band < us.m_blocks) {
+      // bands of m_band row blocks, each walked over all column groups
+      const int band_units = p.m_band * p.n_groups;
+      const int band = u / band_units;
+      const int ub = u - band * band_units;
+      const int mb0 = band * p.m_band;
+      const int mbn = min(p.m_band, us.m_blocks - mb0);
+      mb = mb0 + ub % mbn;
+      g = ub / mbn;
+    } else {
+      mb = u % us.m_blocks;
+      g = u / us.m_blocks;
+    }
   } else {
     g = u % p.n_groups;
     mb = u / p.n_groups;
