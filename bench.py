@@ -50,6 +50,8 @@ def parse_args():
     ap.add_argument("--reference-rows", type=int, default=128,
                     help="token rows per oracle step of --impl reference")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--copy-streams", type=int, default=4,
+                    help="end-to-end leg: copy streams per direction (large copies are split)")
     ap.add_argument("--summarize-traffic", metavar="NCU_CSV", default=None,
                     help="write profiles/traffic_<workload>.txt from an ncu --csv capture of "
                          "dram__bytes_read.sum / dram__bytes_write.sum over one step, then exit")
@@ -430,18 +432,39 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                           "nv": torch.empty_like(nv),
                           "ev_in": torch.cuda.Event(), "ev_comp": torch.cuda.Event(),
                           "ev_out": torch.cuda.Event()})
-        s_up = torch.cuda.Stream(dev)
-        s_down = torch.cuda.Stream(dev)
+        ncs = max(1, args.copy_streams)
+        ups = [torch.cuda.Stream(dev) for _ in range(ncs)]
+        downs = [torch.cuda.Stream(dev) for _ in range(ncs)]
+        s_up, s_down = ups[0], downs[0]
+
+        def split_copy(dsts, srcs, streams, wait_ev, done_ev):
+            """dst.copy_(src) for each pair, large tensors cut in row pieces spread
+            over the streams; done_ev (on streams[0]) fires when all are done."""
+            pieces = []
+            for d, s_ in zip(dsts, srcs):
+                n = d.shape[0] if d.dim() else 1
+                cut = min(len(streams), n) if d.numel() * d.element_size() > (64 << 20) else 1
+                step_rows = (n + cut - 1) // cut
+                for i in range(cut):
+                    pieces.append((d[i * step_rows:(i + 1) * step_rows],
+                                   s_[i * step_rows:(i + 1) * step_rows]) if cut > 1 else (d, s_))
+            evs = []
+            for j, (d, s_) in enumerate(pieces):
+                st = streams[j % len(streams)]
+                with torch.cuda.stream(st):
+                    st.wait_event(wait_ev)
+                    d.copy_(s_, non_blocking=True)
+            for st in streams[1:]:
+                e = torch.cuda.Event()
+                e.record(st)
+                streams[0].wait_event(e)
+            done_ev.record(streams[0])
 
         def e2e_step(k):
             sl = slots[k % 2]
             xd, wd, yd = sl["in"]
-            with torch.cuda.stream(s_up):
-                s_up.wait_event(sl["ev_comp"])      # step k-2 no longer reads these inputs
-                xd.copy_(Xp, non_blocking=True)
-                wd.copy_(Wp, non_blocking=True)
-                yd.copy_(yp, non_blocking=True)
-                sl["ev_in"].record(s_up)
+            # step k-2 no longer reads these inputs once its fused call is done
+            split_copy((xd, wd, yd), (Xp, Wp, yp), ups, sl["ev_comp"], sl["ev_in"])
             stream.wait_event(sl["ev_in"])
             stream.wait_event(sl["ev_out"])         # step k-2's outputs are downloaded
             lo, ls, dx, dw = sl["out"]
@@ -450,11 +473,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                            workspace_buf=ws, err_word=err, stream=stream, z_loss=args.z_loss,
                            skip_ignored_blocks=args.skip_ignored, grad_filter=args.grad_filter)
             sl["ev_comp"].record(stream)
-            with torch.cuda.stream(s_down):
-                s_down.wait_event(sl["ev_comp"])
-                for h, d in zip(sl["host"], sl["out"]):
-                    h.copy_(d, non_blocking=True)
-                sl["ev_out"].record(s_down)
+            split_copy(sl["host"], sl["out"], downs, sl["ev_comp"], sl["ev_out"])
 
         for k in range(max(args.warmup, 2)):
             e2e_step(k)
@@ -478,7 +497,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         e2e = {"value": world * N * args.steps / (ems / 1e3), "unit": "tokens/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": ems / args.steps, "loss_read_back": host_loss,
-               "overlap": "uploads and downloads of neighbouring steps overlap the fused call"}
+               "overlap": "uploads and downloads of neighbouring steps overlap the fused call",
+               "copy_streams_per_direction": ncs}
 
     if rank != 0:
         return
