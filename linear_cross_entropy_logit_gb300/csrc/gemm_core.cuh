@@ -249,6 +249,81 @@ __device__ __forceinline__ void staging_write_row(uint32_t buf, int row, const u
   }
 }
 
+// Per-row constants of the dZ epilogue: dZ = pcoef * p - eps_v - tgt * 1[j = y]
+// with p = exp2(z * log2(e) + neg_lse2), c = grad / N_valid, valid = 0 for
+// ignored and padding rows.
+struct DzRow {
+  float pcoef;     // c * valid * (1 + 2 alpha lse)
+  float neg_lse2;  // -lse * log2(e)
+  float eps_v;     // c * valid * eps / V
+  float tgt;       // c * valid * (1 - eps)
+};
+
+__device__ __forceinline__ DzRow dz_row(bool valid, float lse_r, float c, float eps, float z_loss,
+                                        int vocab) {
+  const float coef = valid ? c : 0.f;
+  return {coef * fmaf(2.f * z_loss, lse_r, 1.f), -lse_r * LOG2E, coef * eps / (float)vocab,
+          coef * (1.f - eps)};
+}
+
+// dZ of one 64-column slice of this thread's row: TMEM columns taddr .. +63 in,
+// 32 packed bf16 pairs out; `off` = label - first column of the slice.
+// Returns the largest probability of the slice when PMAX (gradient filtering).
+template <bool PMAX>
+__device__ __forceinline__ float dz_slice(uint32_t taddr, const DzRow& d, long long off,
+                                          uint32_t (&w)[32]) {
+  uint32_t r0[32], r1[32];
+  tmem_ld_32x32b_x32(taddr, r0);
+  tmem_ld_32x32b_x32(taddr + 32, r1);
+  tmem_ld_wait_regs(r0);
+  tmem_ld_wait_regs(r1);
+  float pmax = 0.f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const float za = __uint_as_float(r0[j]);
+    const float zb = __uint_as_float(r1[j]);
+    const float pa = ex2_approx(fmaf(za, LOG2E, d.neg_lse2));
+    const float pb = ex2_approx(fmaf(zb, LOG2E, d.neg_lse2));
+    if constexpr (PMAX) pmax = fmaxf(pmax, fmaxf(pa, pb));
+    float da = fmaf(d.pcoef, pa, -d.eps_v);
+    float db = fmaf(d.pcoef, pb, -d.eps_v);
+    if (off == j) da -= d.tgt;
+    if (off == j + 32) db -= d.tgt;
+    r0[j] = __float_as_uint(da);
+    r1[j] = __float_as_uint(db);
+  }
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    w[j] = pack_bf16x2(__uint_as_float(r0[2 * j]), __uint_as_float(r0[2 * j + 1]));
+    w[16 + j] = pack_bf16x2(__uint_as_float(r1[2 * j]), __uint_as_float(r1[2 * j + 1]));
+  }
+  return pmax;
+}
+
+// One warp writes its 32 rows x 128 bytes (one row per lane) through a
+// swizzled staging buffer and lane 0 stores (or reduce-adds) the box at
+// (c0, row0) by TMA.  Each warp alternates its two buffers by a running count
+// of its stores (not by the slice index: a clipped tile can end on either
+// buffer), so the buffer written now was last read by the store before the
+// latest one, and waiting until at most one store is still reading suffices.
+__device__ __forceinline__ void staged_store(uint32_t buf, uint8_t* staging, int lane,
+                                             const uint32_t* w, const CUtensorMap* out, int c0,
+                                             int row0, bool reduce_add) {
+  if (lane == 0) bulk_wait_group_read<1>();
+  __syncwarp();
+  staging_write_row(buf, lane, w);
+  fence_proxy_async_shared();
+  __syncwarp();
+  if (lane == 0) {
+    const void* src = staging + (buf - smem_u32(staging));
+    if (reduce_add)
+      tma_reduce_add_2d(out, src, c0, row0);
+    else
+      tma_store_2d(out, src, c0, row0);
+    bulk_commit_group();
+  }
+}
+
 template <Epi EPI, bool A_MN, bool B_MN, int STAGES, bool PAIR, bool EXT>
 __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensorMap& tmB,
                                           const CUtensorMap& tmOut, const GemmParams& p) {
@@ -525,6 +600,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     const uint32_t stag0 = smem_u32(staging) + (warp - 2) * 2 * STAGING_BUF_BYTES;
     uint32_t tile = 0;
+    uint32_t nstore = 0;  // this warp's staged stores so far: buffer nstore & 1
     bool ok = true;
     float c_scale = 0.f;
     if constexpr (EPI == Epi::kDz) c_scale = *p.scale;
@@ -544,15 +620,9 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
       const bool valid = row_ok && label != p.ignore_index;
       const long long lab_rel = label - p.col_base;
 
-      float dz_coef = 0.f, dz_pcoef = 0.f, dz_neg_lse2 = 0.f, dz_eps = 0.f, dz_tgt = 0.f;
-      if constexpr (EPI == Epi::kDz) {
-        const float lse_r = row_ok ? p.lse[row] : 0.f;
-        dz_coef = valid ? c_scale : 0.f;
-        dz_pcoef = dz_coef * fmaf(2.f * p.z_loss, lse_r, 1.f);
-        dz_neg_lse2 = -lse_r * LOG2E;
-        dz_eps = dz_coef * p.smoothing / (float)p.vocab;
-        dz_tgt = dz_coef * (1.f - p.smoothing);
-      }
+      DzRow dzr{};
+      if constexpr (EPI == Epi::kDz)
+        dzr = dz_row(valid, row_ok ? p.lse[row] : 0.f, c_scale, p.smoothing, p.z_loss, p.vocab);
 
       for (int nb = nb0; nb < nb1; ++nb) {
         const uint32_t acc = tile & 1u;
@@ -606,28 +676,9 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
           for (int sl = 0; sl < BN / 64; ++sl) {
             const int c0 = nb * BN + sl * 64;
             if (c0 >= p.col_limit) break;  // warp-uniform; the store would be clipped anyway
-            uint32_t r0[32], r1[32];
-            tmem_ld_32x32b_x32(taddr + sl * 64, r0);
-            tmem_ld_32x32b_x32(taddr + sl * 64 + 32, r1);
-            tmem_ld_wait_regs(r0);
-            tmem_ld_wait_regs(r1);
-            uint32_t w[32];
             const long long off = lab_rel - c0;
-            float pmax = 0.f;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float za = __uint_as_float(r0[j]);
-              const float zb = __uint_as_float(r1[j]);
-              const float pa = ex2_approx(fmaf(za, LOG2E, dz_neg_lse2));
-              const float pb = ex2_approx(fmaf(zb, LOG2E, dz_neg_lse2));
-              if constexpr (EXT) pmax = fmaxf(pmax, fmaxf(pa, pb));
-              float da = fmaf(dz_pcoef, pa, -dz_eps);
-              float db = fmaf(dz_pcoef, pb, -dz_eps);
-              if (off == j) da -= dz_tgt;
-              if (off == j + 32) db -= dz_tgt;
-              r0[j] = __float_as_uint(da);
-              r1[j] = __float_as_uint(db);
-            }
+            uint32_t w[32];
+            const float pmax = dz_slice<EXT>(taddr + sl * 64, dzr, off, w);
             if (EXT && p.mask_x_out) {
               // this 32-token x 64-column block is kept if a valid row has a
               // probability >= the threshold or its target in it
@@ -637,21 +688,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
                 p.mask_w_out[(size_t)(c0 / p.mask_tile) * p.mask_w_ld + store_row0 / 64] = 1;
               }
             }
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              w[j] = pack_bf16x2(__uint_as_float(r0[2 * j]), __uint_as_float(r0[2 * j + 1]));
-              w[16 + j] = pack_bf16x2(__uint_as_float(r1[2 * j]), __uint_as_float(r1[2 * j + 1]));
-            }
-            const uint32_t buf = stag0 + (sl & 1) * STAGING_BUF_BYTES;
-            if (lane == 0) bulk_wait_group_read<1>();
-            __syncwarp();
-            staging_write_row(buf, lane, w);
-            fence_proxy_async_shared();
-            __syncwarp();
-            if (lane == 0) {
-              tma_store_2d(&tmOut, staging + (buf - smem_u32(staging)), c0, store_row0);
-              bulk_commit_group();
-            }
+            staged_store(stag0 + (nstore++ & 1u) * STAGING_BUF_BYTES, staging, lane, w, &tmOut,
+                         c0, store_row0, false);
           }
         } else {  // kStore
 #pragma unroll 1
@@ -665,20 +703,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
 #pragma unroll
               for (int j = 0; j < 32; ++j) r[j] = 0u;
             }
-            const uint32_t buf = stag0 + (sl & 1) * STAGING_BUF_BYTES;
-            if (lane == 0) bulk_wait_group_read<1>();
-            __syncwarp();
-            staging_write_row(buf, lane, r);
-            fence_proxy_async_shared();
-            __syncwarp();
-            if (lane == 0) {
-              const void* src = staging + (buf - smem_u32(staging));
-              if (p.reduce_add)
-                tma_reduce_add_2d(&tmOut, src, c0, store_row0);
-              else
-                tma_store_2d(&tmOut, src, c0, store_row0);
-              bulk_commit_group();
-            }
+            staged_store(stag0 + (nstore++ & 1u) * STAGING_BUF_BYTES, staging, lane, r, &tmOut,
+                         c0, store_row0, p.reduce_add != 0);
           }
         }
 
