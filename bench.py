@@ -68,10 +68,13 @@ def parse_args():
                     help="z-loss weight alpha (adds alpha * lse^2 per valid token)")
     ap.add_argument("--single-cta", action="store_true",
                     help="128x256 single-CTA tiles instead of 256x256 CTA-pair tiles")
+    ap.add_argument("--merge", action="store_true",
+                    help="one merged dW(c) + dX(c) + dZ(c+1) backward launch per vocabulary "
+                         "chunk (two dZ buffers) instead of three launches")
     return ap.parse_args()
 
 
-KERNEL_SOURCES = ("gemm_core.cuh", "ptx.cuh", "aux_kernels.cuh", "flce_api.cu")
+KERNEL_SOURCES = ("gemm_core.cuh", "bwd_fused.cuh", "ptx.cuh", "aux_kernels.cuh", "flce_api.cu")
 KIND_BY_EPI = {("0", None): "fwd_logits_lse", ("1", None): "bwd_dz_recompute",
                ("2", "1"): "bwd_dw_gemm", ("2", "0"): "bwd_dx_gemm"}
 
@@ -101,9 +104,12 @@ def summarize_traffic(csv_path: str, workload: str) -> None:
         name = r["Kernel Name"]
         m = (re.search(r"EpiE(\d)ELb(\d)ELb(\d)", name)
              or re.search(r"gemm_(?:pair_)?kernel<(\d), (\d), (\d), \d+(?:, \d)?>", name))
-        if not m:
+        if "bwd_fused_kernel" in name:
+            kind = "bwd_merged"
+        elif m:
+            kind = KIND_BY_EPI.get((m.group(1), None)) or KIND_BY_EPI[(m.group(1), m.group(2))]
+        else:
             continue
-        kind = KIND_BY_EPI.get((m.group(1), None)) or KIND_BY_EPI[(m.group(1), m.group(2))]
         d = per.setdefault(kind, {"ids": set(), "read": 0.0, "write": 0.0})
         d["ids"].add(r["ID"])
         scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}.get(r["Metric Unit"], None)
@@ -268,6 +274,28 @@ def workload_spec(args):
     return spec
 
 
+def kind_flops(B, N, H, V, args, merged):
+    """Algorithmic FLOP per step of each profiled kernel kind.
+
+    Forward, dZ recompute, dW and dX each contract 2*N*V*H per step.  With
+    merged backward launches the dZ kind runs only chunk 0 of each backward
+    call (2*N*w0*H) and the merged kind the rest of the three backward
+    contractions (6*N*V*H minus that)."""
+    calls = [V]
+    if args.vocab_shards > 1:
+        P = args.vocab_shards
+        bounds = [round(V * i / P / 256) * 256 for i in range(P)] + [V]
+        calls = [b1 - b0 for b0, b1 in zip(bounds, bounds[1:])]
+    full = 2.0 * N * V * H
+    out = {"fwd_logits_lse": full, "bwd_dz_recompute": full, "bwd_dw_gemm": full,
+           "bwd_dx_gemm": full, "bwd_merged": 0.0}
+    if merged:
+        dz0 = sum(2.0 * N * min(B.flce_vocab_chunk(N, v), v) * H for v in calls)
+        out["bwd_dz_recompute"] = dz0
+        out["bwd_merged"] = 3.0 * full - dz0
+    return out
+
+
 def workload_config(spec, chunk):
     cfg = {"workload": spec.name, "N": spec.N, "H": spec.H, "V": spec.V,
            "inputs": f"X {spec.dtype} N(0,{spec.x_std}^2)"
@@ -308,6 +336,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     B.flce_set_vocab_chunk(args.vocab_chunk)
     B.flce_set_l2_hints(args.l2_hints)
     B.flce_set_cta_pair(not args.single_cta)
+    B.flce_set_backward_merge(args.merge)
     chunk = B.flce_vocab_chunk(N, V)
 
     def host_tensor(a):
@@ -526,18 +555,20 @@ def run_ours(args, rank: int, world: int, local_rank: int):
 
     # dominant kernel: largest share of the profiled device time
     kinds = {}
-    flops_kind = 2.0 * N * V * H  # each kind performs one 2NVH contraction per step
+    flops_kind = kind_flops(B, N, H, V, args, merged=prof["bwd_merged"][1] > 0)
     total_prof_ms = sum(v[0] for v in prof.values()) or 1.0
     for name, (kms, n) in prof.items():
         if n == 0:
             continue
         kinds[name] = {"launches": n, "ms_total": kms, "ms_per_launch": kms / n,
                        "share_of_gemm_time": kms / total_prof_ms,
-                       "tflops": flops_kind * args.steps / (kms / 1e3) / 1e12}
+                       "flops_per_step": flops_kind[name],
+                       "tflops": flops_kind[name] * args.steps / (kms / 1e3) / 1e12}
     dom = max(kinds, key=lambda k: kinds[k]["ms_total"]) if kinds else None
     roofline = None
     dense_default = not (args.skip_ignored or args.grad_filter or args.vocab_shards > 1 or
-                         args.shape or args.single_cta or args.l2_hints)
+                         args.shape or args.single_cta or args.l2_hints or args.merge or
+                         args.vocab_chunk)
     traffic = load_traffic(spec.name) if dense_default else None
     if dom:
         ach = kinds[dom]["tflops"]
@@ -558,6 +589,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     extra = {"workspace_bytes": ws.numel(),
              "workspace_vs_nxv_bf16": ws.numel() / (N * V * 2),
              "dz_chunk_bytes": N * chunk * 2,
+             "dz_buffers": 2 if (B.flce_backward_merge() and B.flce_cta_pair()) else 1,
              "peak_extra_device_bytes": peak_extra,
              "nxv_bf16_bytes": N * V * 2}
     line = {
@@ -569,6 +601,10 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                        l2="inputs larger than L2 (W alone is %.2f GB)" % (V * H * elem / 1e9),
                        parallelism=f"replicas x{world} (each rank its own batch, no collective)",
                        tiles="128x256 single CTA" if args.single_cta else "256x256 CTA pair",
+                       backward="merged dW(c) + dX(c) + dZ(c+1) launch per vocabulary chunk"
+                       if (args.merge and not (args.single_cta or args.skip_ignored
+                                               or args.grad_filter or args.l2_hints))
+                       else "three launches per vocabulary chunk",
                        z_loss=args.z_loss,
                        skip_ignored_blocks=args.skip_ignored,
                        grad_filter=args.grad_filter or None,

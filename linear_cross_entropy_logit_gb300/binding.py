@@ -39,10 +39,11 @@ EXPORTED = (
     "flce_set_cta_pair", "flce_cta_pair", "flce_set_l2_hints", "flce_options_init",
     "flce_forward_ex", "flce_backward_ex", "flce_fwd_bwd_ex", "flce_forward_vocab_shard",
     "flce_combine_workspace_size", "flce_combine_vocab_shards", "flce_backward_vocab_shard",
-    "flce_debug_wait_timeout",
+    "flce_debug_wait_timeout", "flce_set_backward_merge", "flce_backward_merge",
 )
 
-PROFILE_KINDS = ("fwd_logits_lse", "bwd_dz_recompute", "bwd_dw_gemm", "bwd_dx_gemm")
+PROFILE_KINDS = ("fwd_logits_lse", "bwd_dz_recompute", "bwd_dw_gemm", "bwd_dx_gemm",
+                 "bwd_merged")
 
 _lib = None
 
@@ -115,6 +116,10 @@ def lib() -> ctypes.CDLL:
     L.flce_cta_pair.restype = I32
     L.flce_set_l2_hints.argtypes = [I32]
     L.flce_set_l2_hints.restype = I32
+    L.flce_set_backward_merge.argtypes = [I32]
+    L.flce_set_backward_merge.restype = I32
+    L.flce_backward_merge.argtypes = []
+    L.flce_backward_merge.restype = I32
     OPT = ctypes.POINTER(FlceOptions)
     L.flce_options_init.argtypes = [OPT]
     L.flce_options_init.restype = None
@@ -207,6 +212,16 @@ def flce_set_l2_hints(on: bool) -> None:
 
 def flce_cta_pair() -> bool:
     return bool(lib().flce_cta_pair())
+
+
+def flce_set_backward_merge(on: bool) -> None:
+    """1: one merged backward launch per vocabulary chunk (two dZ buffers);
+    0: three launches per chunk (default)."""
+    _check(lib().flce_set_backward_merge(int(bool(on))), "flce_set_backward_merge")
+
+
+def flce_backward_merge() -> bool:
+    return bool(lib().flce_backward_merge())
 
 
 def flce_vocab_chunk(N: int, V: int) -> int:

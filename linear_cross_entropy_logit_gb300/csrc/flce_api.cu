@@ -8,6 +8,10 @@
 //                                      gemm<kStore> dW[v0:v0+Cv] = dZ^T X
 //                                      gemm<kStore> dX_acc += dZ W[v0:v0+Cv]
 //                      then dx_finalize (bf16 inputs).
+// Merged backward (opt-in, CTA-pair tiles without the optional features):
+// gemm<kDz> for chunk 0 alone, then one bwd_fused launch per chunk c running
+// dW(c), dX(c) and the dZ recompute of chunk c+1 from one tile list; the dZ
+// scratch is two N x Cv buffers used in turn.
 // Running the vocabulary chunks outermost lets the dW GEMM contract over all
 // N tokens at once, so every dW row is written exactly once per call (no
 // read-modify-write of the V x H fp32 gradient), while the N x Cv bf16
@@ -28,6 +32,7 @@
 
 #include "flce.h"
 #include "aux_kernels.cuh"
+#include "bwd_fused.cuh"
 #include "gemm_core.cuh"
 #include "ptx.cuh"
 
@@ -38,7 +43,7 @@ namespace {
 constexpr int kStages = 4;       // 1-CTA tiles: 4 x 48 KB stages
 constexpr int kPairStages = 6;   // CTA-pair tiles: 6 x 32 KB stages per CTA
 constexpr int64_t kPartialsBudget = 32ll << 20;   // bytes of forward partials
-constexpr int64_t kDzBudget = 256ll << 20;        // bytes of the dZ chunk (default)
+constexpr int64_t kDzBudget = 256ll << 20;        // bytes of all dZ chunk buffers (default)
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
 constexpr size_t kAlign = 256;
 
@@ -46,10 +51,12 @@ thread_local std::string g_last_cuda_error;
 thread_local int g_launches = 0;
 std::atomic<int64_t> g_vocab_chunk{0};
 std::atomic<int> g_cta_pair{1};
+std::atomic<int> g_bwd_merge{0};
 
 // Optional per-kernel timing: CUDA events recorded on the caller's stream
-// around every GEMM launch (kinds: forward logits+LSE, dZ recompute, dW, dX).
-constexpr int kProfKinds = 4;
+// around every GEMM launch (kinds: forward logits+LSE, dZ recompute, dW, dX,
+// merged backward).
+constexpr int kProfKinds = 5;
 struct ProfRec {
   int kind;
   cudaEvent_t start, stop;
@@ -57,8 +64,8 @@ struct ProfRec {
 thread_local bool g_prof_on = false;
 thread_local std::vector<ProfRec> g_prof_pending;
 thread_local std::vector<cudaEvent_t> g_prof_pool;
-thread_local double g_prof_ms[kProfKinds] = {0, 0, 0, 0};
-thread_local int g_prof_n[kProfKinds] = {0, 0, 0, 0};
+thread_local double g_prof_ms[kProfKinds] = {};
+thread_local int g_prof_n[kProfKinds] = {};
 
 cudaEvent_t prof_event() {
   if (!g_prof_pool.empty()) {
@@ -95,8 +102,9 @@ struct Plan {
   int m_blocks, m_pad, v_tiles, group_len, n_groups, merge_blocks;
   int64_t chunk;
   int n_chunks;
+  int dz_bufs;  // 2 when the merged backward may run (dZ of chunk c+1 beside chunk c)
   size_t off_scalars, off_blocks, off_partials, off_block_loss, off_block_valid, off_dz,
-      off_dxacc, off_xcast, off_wcast, off_mask_x, off_mask_w, total;
+      off_dz2, off_counters, off_dxacc, off_xcast, off_wcast, off_mask_x, off_mask_w, total;
   // gradient-filter masks (sized for 128-row tiles, the smaller tile shape)
   int mask_x_ld, mask_w_ld;
   int n_blocks128;  // token blocks of 128 rows (the finest skip granularity)
@@ -111,14 +119,21 @@ bool shape_ok(int64_t N, int64_t H, int64_t V) {
   return true;
 }
 
+// Whether backward calls may take the merged launches (CTA-pair tiles only);
+// their workspace then holds two dZ buffers.
+bool merge_planned() { return g_bwd_merge.load() != 0 && g_cta_pair.load() != 0; }
+int dz_buffers() { return merge_planned() ? 2 : 1; }
+
+// Cv: the dZ buffers together take at most kDzBudget (default) and at most
+// half of the N x V logits (each buffer at most V / (2 * buffers) columns).
 int64_t auto_chunk(int64_t N, int64_t V) {
-  const int64_t half = std::max<int64_t>(256, (V / 2) / 256 * 256);
+  const int64_t half = std::max<int64_t>(256, (V / (2 * dz_buffers())) / 256 * 256);
   int64_t set = g_vocab_chunk.load();
   int64_t c;
   if (set > 0) {
     c = ceil_div(set, 256) * 256;
   } else {
-    c = (kDzBudget / (std::max<int64_t>(N, 1) * 2)) / 256 * 256;
+    c = (kDzBudget / dz_buffers() / (std::max<int64_t>(N, 1) * 2)) / 256 * 256;
   }
   return std::min(std::max<int64_t>(c, 256), half);
 }
@@ -141,6 +156,7 @@ bool make_plan(int64_t N, int64_t H, int64_t V, flce_dtype dtype, int mode, Plan
   p.merge_blocks = (int)ceil_div(std::max<int64_t>(N, 1), MERGE_THREADS);
   p.chunk = auto_chunk(N, V);
   p.n_chunks = (int)ceil_div(V, p.chunk);
+  p.dz_bufs = dz_buffers();
   const bool fwd = mode & FLCE_MODE_FWD;
   const bool bwd = mode & FLCE_MODE_BWD;
   size_t off = 0;
@@ -159,10 +175,16 @@ bool make_plan(int64_t N, int64_t H, int64_t V, flce_dtype dtype, int mode, Plan
     p.off_block_valid = off;
     off = align_up(off + (size_t)p.merge_blocks * sizeof(int), kAlign);
   }
-  p.off_dz = p.off_dxacc = 0;
+  p.off_dz = p.off_dz2 = p.off_counters = p.off_dxacc = 0;
   if (bwd) {
     p.off_dz = off;
     off = align_up(off + (size_t)std::max<int64_t>(N, 1) * p.chunk * 2, kAlign);
+    if (p.dz_bufs == 2) {
+      p.off_dz2 = off;
+      off = align_up(off + (size_t)std::max<int64_t>(N, 1) * p.chunk * 2, kAlign);
+      p.off_counters = off;  // one tile counter per merged launch
+      off = align_up(off + (size_t)p.n_chunks * sizeof(int), kAlign);
+    }
     if (dtype == FLCE_BF16) {
       p.off_dxacc = off;
       off = align_up(off + (size_t)N * H * 4, kAlign);
@@ -342,6 +364,50 @@ flce_status launch_tile(bool pair, bool ext, int dev, int num_sms, const CUtenso
 }
 
 bool use_pair() { return g_cta_pair.load() != 0; }
+
+// One merged backward launch (CTA pairs, persistent; the list's tiles go round
+// robin except the last DYNAMIC_ROUNDS rounds, taken from a global counter).
+flce_status launch_fused(int dev, int num_sms, const FusedMaps& maps, const FusedParams& p,
+                         cudaStream_t st) {
+  constexpr int smem = fused_smem_bytes<kPairStages>();
+  auto kern = bwd_fused_kernel<kPairStages>;
+  static std::once_flag flags[kMaxDevices];
+  cudaError_t attr_err = cudaSuccess;
+  std::call_once(flags[dev], [&] {
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  });
+  if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute");
+  if (p.total_tiles <= 0) return FLCE_OK;
+  static int max_clusters[kMaxDevices] = {0};
+  if (max_clusters[dev] == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    int n = 0;
+    FLCE_CUDA(cudaOccupancyMaxActiveClusters(&n, kern, &cfg));
+    max_clusters[dev] = std::max(1, std::min(n, num_sms / 2));
+  }
+  const int pairs = std::min(p.total_tiles, max_clusters[dev]);
+  const int grid = 2 * pairs;
+  // all but the last DYNAMIC_ROUNDS rounds of tiles go round robin
+  FusedParams pp = p;
+  pp.static_tiles = std::max(0, (p.total_tiles - DYNAMIC_ROUNDS * pairs) / pairs * pairs);
+  ProfRec rec{4, nullptr, nullptr};
+  if (g_prof_on) {
+    rec.start = prof_event();
+    rec.stop = prof_event();
+    if (rec.start && rec.stop) FLCE_CUDA(cudaEventRecord(rec.start, st));
+  }
+  kern<<<grid, NUM_THREADS, smem, st>>>(maps, pp);
+  ++g_launches;
+  FLCE_CUDA(cudaGetLastError());
+  if (rec.start && rec.stop) {
+    FLCE_CUDA(cudaEventRecord(rec.stop, st));
+    g_prof_pending.push_back(rec);
+  }
+  return FLCE_OK;
+}
 
 // Row-block bands for the launches that re-read X (forward, dZ recompute):
 // with all row blocks in flight, X (N x H bf16) competes in L2 with the
@@ -584,23 +650,8 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
   uint8_t* mask_w = ws + pl.off_mask_w;
   const size_t mask_x_bytes = (size_t)ceil_div(N, BM) * pl.mask_x_ld;
   const size_t mask_w_bytes = (size_t)ceil_div(Cv, BM) * pl.mask_w_ld;
-  for (int ci = 0; ci < pl.n_chunks; ++ci) {
-    const int64_t v0 = (int64_t)ci * Cv;
-    const int64_t w = std::min(Cv, V - v0);
-    if (filt) {
-      FLCE_CUDA(cudaMemsetAsync(mask_x, 0, mask_x_bytes, c.st));
-      FLCE_CUDA(cudaMemsetAsync(mask_w, 0, mask_w_bytes, c.st));
-    }
-    const void* Wc = Wb16 + v0 * H;
-    CUtensorMap tmWc_k, tmWc_mn, tmDzSt, tmDz_mn, tmDz_k, tmDw;
-    FLCE_TRY(map_kmajor(&tmWc_k, Wc, H, w, H, b_box_rows(pair)));
-    FLCE_TRY(map_mnmajor(&tmWc_mn, Wc, H, w, H));
-    FLCE_TRY(map_dz_store(&tmDzSt, dz, w, N, Cv));
-    FLCE_TRY(map_mnmajor(&tmDz_mn, dz, w, N, Cv));
-    FLCE_TRY(map_kmajor(&tmDz_k, dz, w, N, Cv, BM));
-    FLCE_TRY(map_f32_out(&tmDw, dW + v0 * H, H, w, H));
-
-    // K3: recompute Z[:, v0:v0+w] and write dZ (bf16) into the chunk scratch.
+  // K3 parameters: recompute Z[:, v0:v0+w] and write dZ (bf16) into a chunk buffer.
+  auto dz_params = [&](int64_t v0, int64_t w) {
     GemmParams p3{};
     p3.m_size = (int)N;
     p3.n_size = (int)w;
@@ -635,59 +686,166 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
     p3.l2_keep_frac = l2_keep_fraction((double)N * H * 2);
     p3.err_word = c.err_word;
     p3.timeout_ns = kTimeoutNs;
-    FLCE_TRY((launch_tile<Epi::kDz, false, false>(pair, ext, dev, sms, tmX_k, tmWc_k, tmDzSt, p3,
-                                                  c.st, 1)));
-
-    // K4: dW[v0:v0+w, :] = dZ_chunk^T X   (K = N tokens)
-    GemmParams p4{};
-    p4.m_size = (int)w;
-    p4.n_size = (int)H;
-    p4.k_size = (int)N;
-    p4.m_blocks = (int)ceil_div(w, tile_rows(pair));
-    p4.n_blocks = h_blocks;
-    p4.group_len = 1;
-    p4.n_groups = h_blocks;
-    p4.num_units = p4.m_blocks * h_blocks;
-    p4.m_fastest = 0;
-    p4.reduce_add = accumulate ? 1 : 0;
-    p4.k_list = sk.list;
-    p4.k_count = sk.count;
-    p4.k_per_entry = tile_rows(pair) / BK;
-    if (filt) {
-      p4.fmask = mask_w;
-      p4.fmask_ld = pl.mask_w_ld;
+    return p3;
+  };
+  if (pair && !ext && pl.dz_bufs == 2) {
+    // Merged backward: dZ of chunk 0 alone, then per chunk c one launch of
+    // dW(c), dX(c) and dZ(c+1), the dZ buffers taken in turn.
+    int* counters = reinterpret_cast<int*>(ws + pl.off_counters);
+    FLCE_CUDA(cudaMemsetAsync(counters, 0, (size_t)pl.n_chunks * sizeof(int), c.st));
+    void* dz_buf[2] = {ws + pl.off_dz, ws + pl.off_dz2};
+    {
+      const int64_t w0 = std::min(Cv, V);
+      CUtensorMap tmW0_k, tmDzSt0;
+      FLCE_TRY(map_kmajor(&tmW0_k, Wb16, H, w0, H, b_box_rows(pair)));
+      FLCE_TRY(map_dz_store(&tmDzSt0, dz_buf[0], w0, N, Cv));
+      FLCE_TRY((launch_tile<Epi::kDz, false, false>(pair, false, dev, sms, tmX_k, tmW0_k, tmDzSt0,
+                                                    dz_params(0, w0), c.st, 1)));
     }
-    p4.l2_keep_b = 1;  // X again; the dZ column block is shared within one wave
-    p4.l2_keep_frac = l2_keep_fraction((double)N * H * 2);
-    p4.err_word = c.err_word;
-    p4.timeout_ns = kTimeoutNs;
-    FLCE_TRY((launch_tile<Epi::kStore, true, true>(pair, ext, dev, sms, tmDz_mn, tmX_mn, tmDw, p4,
-                                                   c.st, 2)));
-
-    // K5: dX_acc (+)= dZ_chunk W[v0:v0+w, :]   (K = w vocabulary columns)
-    GemmParams p5{};
-    p5.m_size = (int)N;
-    p5.n_size = (int)H;
-    p5.k_size = (int)w;
-    p5.m_blocks = m_blocks_tok;
-    p5.n_blocks = h_blocks;
-    p5.group_len = 1;
-    p5.n_groups = h_blocks;
-    p5.num_units = m_blocks_tok * h_blocks;
-    p5.m_fastest = 0;
-    p5.reduce_add = ci > 0 ? 1 : 0;
-    p5.row_list = sk.list;
-    p5.row_count = sk.count;
-    if (filt) {
-      p5.fmask = mask_x;
-      p5.fmask_ld = pl.mask_x_ld;
+    for (int ci = 0; ci < pl.n_chunks; ++ci) {
+      const int64_t v0 = (int64_t)ci * Cv;
+      const int64_t w = std::min(Cv, V - v0);
+      const bool next = ci + 1 < pl.n_chunks;
+      const int64_t v1 = v0 + Cv;
+      const int64_t w1 = next ? std::min(Cv, V - v1) : 0;
+      const void* cur = dz_buf[ci & 1];
+      const void* Wc = Wb16 + v0 * H;
+      FusedMaps fm;
+      FLCE_TRY(map_mnmajor(&fm.a[kFusedDw], cur, w, N, Cv));
+      fm.b[kFusedDw] = tmX_mn;
+      FLCE_TRY(map_f32_out(&fm.out[kFusedDw], dW + v0 * H, H, w, H));
+      FLCE_TRY(map_kmajor(&fm.a[kFusedDx], cur, w, N, Cv, BM));
+      FLCE_TRY(map_mnmajor(&fm.b[kFusedDx], Wc, H, w, H));
+      fm.out[kFusedDx] = tmDxAcc;
+      fm.a[kFusedDz] = tmX_k;
+      if (next) {
+        FLCE_TRY(map_kmajor(&fm.b[kFusedDz], Wb16 + v1 * H, H, w1, H, b_box_rows(pair)));
+        FLCE_TRY(map_dz_store(&fm.out[kFusedDz], dz_buf[(ci + 1) & 1], w1, N, Cv));
+      } else {  // no dZ tiles: valid maps for the prefetch only
+        fm.b[kFusedDz] = tmX_k;
+        fm.out[kFusedDz] = tmX_k;
+      }
+      FusedSeg segs[3];
+      int n_seg = 0;
+      auto seg = [&](int kind, int m_size, int n_size, int k_size, int m_fastest, int m_band,
+                     int reduce_add) {
+        FusedSeg g{};
+        g.kind = kind;
+        g.m_size = m_size;
+        g.n_size = n_size;
+        g.k_size = k_size;
+        g.m_blocks = (int)ceil_div(m_size, 2 * BM);
+        g.n_blocks = (int)ceil_div(n_size, BN);
+        g.num_tiles = g.m_blocks * g.n_blocks;
+        g.m_fastest = m_fastest;
+        g.m_band = m_band;
+        g.reduce_add = reduce_add;
+        segs[n_seg++] = g;
+      };
+      // dX first among equals: its tiles hold a whole row block of dX_acc
+      seg(kFusedDx, (int)N, (int)H, (int)w, 0, 0, ci > 0 ? 1 : 0);
+      seg(kFusedDw, (int)w, (int)H, (int)N, 0, 0, accumulate ? 1 : 0);
+      if (next) seg(kFusedDz, (int)N, (int)w1, (int)H, 1, x_band(N, H, m_blocks_tok), 0);
+      // longest k-loop first, so the list ends on the shortest tiles
+      std::stable_sort(segs, segs + n_seg, [](const FusedSeg& a, const FusedSeg& b) {
+        return ceil_div(a.k_size, BK) > ceil_div(b.k_size, BK);
+      });
+      FusedParams fp{};
+      int first = 0;
+      for (int i = 0; i < n_seg; ++i) {
+        segs[i].first = first;
+        first += segs[i].num_tiles;
+        fp.seg[i] = segs[i];
+      }
+      fp.n_seg = n_seg;
+      fp.total_tiles = first;
+      fp.tile_counter = counters + ci;
+      fp.labels = c.labels;
+      fp.ignore_index = c.ignore_index;
+      fp.vocab = (int)c.vocab_total;
+      fp.col_base = (int)(c.vocab_offset + v1);
+      fp.col_limit = (int)w1;
+      fp.smoothing = c.smoothing;
+      fp.z_loss = c.z_loss;
+      fp.lse = lse;
+      fp.scale = scale;
+      fp.err_word = c.err_word;
+      fp.timeout_ns = kTimeoutNs;
+      FLCE_TRY(launch_fused(dev, sms, fm, fp, c.st));
     }
-    p5.l2_keep_b = 1;  // the W chunk; the dZ row block is shared within one wave
-    p5.l2_keep_frac = l2_keep_fraction((double)w * H * 2);
-    p5.err_word = c.err_word;
-    p5.timeout_ns = kTimeoutNs;
-    FLCE_TRY((launch_tile<Epi::kStore, false, true>(pair, ext, dev, sms, tmDz_k, tmWc_mn, tmDxAcc,
-                                                    p5, c.st, 3)));
+  } else {
+    for (int ci = 0; ci < pl.n_chunks; ++ci) {
+      const int64_t v0 = (int64_t)ci * Cv;
+      const int64_t w = std::min(Cv, V - v0);
+      if (filt) {
+        FLCE_CUDA(cudaMemsetAsync(mask_x, 0, mask_x_bytes, c.st));
+        FLCE_CUDA(cudaMemsetAsync(mask_w, 0, mask_w_bytes, c.st));
+      }
+      const void* Wc = Wb16 + v0 * H;
+      CUtensorMap tmWc_k, tmWc_mn, tmDzSt, tmDz_mn, tmDz_k, tmDw;
+      FLCE_TRY(map_kmajor(&tmWc_k, Wc, H, w, H, b_box_rows(pair)));
+      FLCE_TRY(map_mnmajor(&tmWc_mn, Wc, H, w, H));
+      FLCE_TRY(map_dz_store(&tmDzSt, dz, w, N, Cv));
+      FLCE_TRY(map_mnmajor(&tmDz_mn, dz, w, N, Cv));
+      FLCE_TRY(map_kmajor(&tmDz_k, dz, w, N, Cv, BM));
+      FLCE_TRY(map_f32_out(&tmDw, dW + v0 * H, H, w, H));
+
+      // K3: recompute Z[:, v0:v0+w] and write dZ (bf16) into the chunk scratch.
+      const GemmParams p3 = dz_params(v0, w);
+      FLCE_TRY((launch_tile<Epi::kDz, false, false>(pair, ext, dev, sms, tmX_k, tmWc_k, tmDzSt,
+                                                    p3, c.st, 1)));
+
+      // K4: dW[v0:v0+w, :] = dZ_chunk^T X   (K = N tokens)
+      GemmParams p4{};
+      p4.m_size = (int)w;
+      p4.n_size = (int)H;
+      p4.k_size = (int)N;
+      p4.m_blocks = (int)ceil_div(w, tile_rows(pair));
+      p4.n_blocks = h_blocks;
+      p4.group_len = 1;
+      p4.n_groups = h_blocks;
+      p4.num_units = p4.m_blocks * h_blocks;
+      p4.m_fastest = 0;
+      p4.reduce_add = accumulate ? 1 : 0;
+      p4.k_list = sk.list;
+      p4.k_count = sk.count;
+      p4.k_per_entry = tile_rows(pair) / BK;
+      if (filt) {
+        p4.fmask = mask_w;
+        p4.fmask_ld = pl.mask_w_ld;
+      }
+      p4.l2_keep_b = 1;  // X again; the dZ column block is shared within one wave
+      p4.l2_keep_frac = l2_keep_fraction((double)N * H * 2);
+      p4.err_word = c.err_word;
+      p4.timeout_ns = kTimeoutNs;
+      FLCE_TRY((launch_tile<Epi::kStore, true, true>(pair, ext, dev, sms, tmDz_mn, tmX_mn, tmDw, p4,
+                                                     c.st, 2)));
+
+      // K5: dX_acc (+)= dZ_chunk W[v0:v0+w, :]   (K = w vocabulary columns)
+      GemmParams p5{};
+      p5.m_size = (int)N;
+      p5.n_size = (int)H;
+      p5.k_size = (int)w;
+      p5.m_blocks = m_blocks_tok;
+      p5.n_blocks = h_blocks;
+      p5.group_len = 1;
+      p5.n_groups = h_blocks;
+      p5.num_units = m_blocks_tok * h_blocks;
+      p5.m_fastest = 0;
+      p5.reduce_add = ci > 0 ? 1 : 0;
+      p5.row_list = sk.list;
+      p5.row_count = sk.count;
+      if (filt) {
+        p5.fmask = mask_x;
+        p5.fmask_ld = pl.mask_x_ld;
+      }
+      p5.l2_keep_b = 1;  // the W chunk; the dZ row block is shared within one wave
+      p5.l2_keep_frac = l2_keep_fraction((double)w * H * 2);
+      p5.err_word = c.err_word;
+      p5.timeout_ns = kTimeoutNs;
+      FLCE_TRY((launch_tile<Epi::kStore, false, true>(pair, ext, dev, sms, tmDz_k, tmWc_mn, tmDxAcc,
+                                                      p5, c.st, 3)));
+    }
   }
   if (c.dtype == FLCE_BF16 && !c.dx_partial_f32) {
     const size_t n4 = (size_t)N * H / 4;
@@ -707,7 +865,7 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
 // ===========================================================================
 extern "C" {
 
-int flce_abi_version(void) { return 103; }
+int flce_abi_version(void) { return 104; }
 
 const char* flce_status_string(flce_status s) {
   switch (s) {
@@ -771,6 +929,13 @@ flce_status flce_set_cta_pair(int on) {
 }
 
 int flce_cta_pair(void) { return g_cta_pair.load(); }
+
+flce_status flce_set_backward_merge(int on) {
+  g_bwd_merge.store(on != 0 ? 1 : 0);
+  return FLCE_OK;
+}
+
+int flce_backward_merge(void) { return g_bwd_merge.load(); }
 
 flce_status flce_set_vocab_chunk(int64_t cols) {
   if (cols < 0) return FLCE_ERR_ARG;

@@ -87,6 +87,40 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
   }
 }
 
+// try_wait with cluster-scope acquire: pairs with a release.cluster arrive by
+// a thread of either CTA of the cluster, so what that thread wrote before
+// arriving (in either CTA's shared memory) is visible after the wait.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar_addr, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar_addr), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// mbar_wait with cluster-scope acquire (same limit and abort handling).
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity,
+                                                  const WaitCtx& ctx) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait_cluster(a, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait_cluster(a, parity)) return true;
+    if ((it & 63u) == 0u) {
+      if (*ctx.abort) return false;
+      if (global_timer_ns() - t0 > ctx.timeout_ns) {
+        *ctx.abort = 1;
+        record_error(ctx.err_word, kErrTimeout);
+        return false;
+      }
+    }
+  }
+}
+
 // Wait used while shutting down after an abort: same limit, but it ignores
 // the abort flag (it is draining this thread's own copies in flight).
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
@@ -306,6 +340,11 @@ __device__ __forceinline__ void cluster_sync_all() {
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];"
                ::"r"(bar_cluster_addr) : "memory");
+}
+
+// 32-bit store into shared memory of either CTA of the cluster.
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 
 // TMA load into this CTA's shared memory whose completion is signalled on an

@@ -21,6 +21,11 @@ def L():
     return binding.lib()
 
 
+def _dz_buffers(B):
+    """dZ buffers a backward workspace holds: two with merged launches."""
+    return 2 if (B.flce_backward_merge() and B.flce_cta_pair()) else 1
+
+
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
@@ -36,7 +41,7 @@ def test_header_exports_all(L):
 
 
 def test_status_strings_and_version(L):
-    assert L.flce_abi_version() == 103
+    assert L.flce_abi_version() == 104
     for s in range(7):
         assert L.flce_status_string(s).decode().startswith("FLCE_")
 
@@ -50,13 +55,15 @@ def test_workspace_plan_bounded():
             continue
         N, H, V = spec.N, spec.H, spec.V
         cv = B.flce_vocab_chunk(N, V)
-        assert cv % 256 == 0 and 256 <= cv <= V // 2
+        bufs = _dz_buffers(B)
+        assert cv % 256 == 0 and 256 <= cv <= V // (2 * bufs)
         nxv = N * V * 2
         ws = B.flce_workspace_size(N, H, V, B.FLCE_BF16, B.MODE_FWD_BWD)
-        # the dZ chunk is the only logit-shaped region and is at most half of N x V
-        assert N * cv * 2 <= nxv // 2
-        # whole workspace: dZ chunk + fp32 dX accumulator + forward partials
-        assert ws <= N * cv * 2 + N * H * 4 + (40 << 20)
+        # the dZ buffers are the only logit-shaped region: together at most
+        # half of N x V and at most 256 MiB
+        assert bufs * N * cv * 2 <= min(nxv // 2, 256 << 20)
+        # whole workspace: dZ buffers + fp32 dX accumulator + forward partials
+        assert ws <= bufs * N * cv * 2 + N * H * 4 + (40 << 20)
         assert ws < nxv
 
 
@@ -69,7 +76,7 @@ def test_workspace_matches_pages_fused_figure():
     fused = [f for f in figs["figures"] if f["N"] == 1024 and f["V"] == 128256][0]
     B.flce_set_vocab_chunk(0)
     cv = B.flce_vocab_chunk(8192, 128256)
-    assert 8192 * cv * 2 / 1e9 <= fused["printed_gb"] + 0.01
+    assert _dz_buffers(B) * 8192 * cv * 2 / 1e9 <= fused["printed_gb"] + 0.01
 
 
 def test_workspace_invalid_shapes():
@@ -81,13 +88,42 @@ def test_workspace_invalid_shapes():
     assert B.flce_workspace_size(0, 16, 100, B.FLCE_BF16, B.MODE_FWD_BWD) > 0
 
 
+def test_backward_merge_setting():
+    """Merged backward (opt-in) plans two dZ buffers and a tile counter per
+    chunk; off (the default), one buffer of twice the width (same total budget)."""
+    from linear_cross_entropy_logit_gb300 import binding as B
+    N, H, V = 8192, 4096, 128256
+    assert not B.flce_backward_merge()
+    B.flce_set_vocab_chunk(0)
+    try:
+        B.flce_set_backward_merge(True)
+        cv2 = B.flce_vocab_chunk(N, V)
+        ws2 = B.flce_workspace_size(N, H, V, B.FLCE_BF16, B.MODE_BWD)
+        B.flce_set_backward_merge(False)
+        cv1 = B.flce_vocab_chunk(N, V)
+        ws1 = B.flce_workspace_size(N, H, V, B.FLCE_BF16, B.MODE_BWD)
+        assert (cv1, cv2) == (16384, 8192)
+        # same dZ bytes; only the tile counters and the filter masks (sized
+        # by Cv) differ
+        assert abs(ws2 - ws1) <= 64 << 10
+        B.flce_set_vocab_chunk(2048)
+        a = B.flce_workspace_size(N, H, V, B.FLCE_BF16, B.MODE_BWD)
+        B.flce_set_backward_merge(True)
+        b = B.flce_workspace_size(N, H, V, B.FLCE_BF16, B.MODE_BWD)
+        assert b - a >= N * 2048 * 2  # a second dZ buffer at the same Cv
+    finally:
+        B.flce_set_backward_merge(False)
+        B.flce_set_vocab_chunk(0)
+
+
 def test_vocab_chunk_setting():
     from linear_cross_entropy_logit_gb300 import binding as B
     try:
         B.flce_set_vocab_chunk(1000)
         assert B.flce_vocab_chunk(8192, 128256) == 1024
         B.flce_set_vocab_chunk(10 ** 9)
-        assert B.flce_vocab_chunk(8192, 128256) == 128256 // 2 // 256 * 256
+        bufs = _dz_buffers(B)
+        assert B.flce_vocab_chunk(8192, 128256) == 128256 // (2 * bufs) // 256 * 256
     finally:
         B.flce_set_vocab_chunk(0)
 
