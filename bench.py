@@ -8,9 +8,10 @@ over one batch of N tokens of the chosen synthetic workload.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 Prints ONE JSON line on rank 0.  ``value`` is tokens/s over all ranks with
-inputs resident in HBM; ``e2e`` is the same metric with the inputs copied
-from pinned host memory and the outputs (loss, lse, dX, dW) copied back inside
-the timed region.  With N > 1 every rank runs its own batch (weak scaling, no
+inputs resident in HBM; ``e2e`` is the same metric with the inputs (X, W,
+labels) copied from pinned host memory and the step's result (the loss) read
+back inside the timed region, and ``e2e_all_outputs`` the same with every
+output (loss, lse, dX, dW) read back.  With N > 1 every rank runs its own batch (weak scaling, no
 collective on the data path).  ``--impl reference`` times the fp64 CPU oracle
 on the host cores instead.
 """
@@ -438,29 +439,15 @@ def run_ours(args, rank: int, world: int, local_rank: int):
 
     # --- end-to-end through the C ABI with host buffers --------------------
     # Every step copies its inputs (X, W, labels) from pinned host memory and
-    # its outputs (loss, lse, dX, dW) back.  Device buffers are double-buffered
-    # so that step k+1's upload and step k-1's download overlap step k's fused
-    # call (three streams ordered by events); the timed region runs from the
-    # first upload to the last download.
-    e2e = None
+    # reads its result back: the loss (the `e2e` key), or with read_all every
+    # output, loss, lse, dX and dW (the `e2e_all_outputs` key).  Device buffers
+    # are double-buffered so that step k+1's upload and step k-1's download
+    # overlap step k's fused call (three streams ordered by events); the timed
+    # region runs from the first upload to the last download.
+    e2e = e2e_all = None
     if not args.no_e2e:
         Xp, Wp, yp = Xh.pin_memory(), Wh.pin_memory(), yh.pin_memory()
         h2d = Xp.numel() * Xp.element_size() + Wp.numel() * Wp.element_size() + yp.numel() * 8
-        d2h = 4 + 4 * N + dX.numel() * dX.element_size() + dW.numel() * 4
-        slots = []
-        for b in range(2):
-            if b == 0:
-                dev_in = (X, W, y)
-                dev_out = (loss, lse, dX, dW)
-            else:
-                dev_in = (torch.empty_like(X), torch.empty_like(W), torch.empty_like(y))
-                dev_out = (torch.empty_like(loss), torch.empty_like(lse), torch.empty_like(dX),
-                           torch.empty_like(dW))
-            host_out = tuple(torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in dev_out)
-            slots.append({"in": dev_in, "out": dev_out, "host": host_out,
-                          "nv": torch.empty_like(nv),
-                          "ev_in": torch.cuda.Event(), "ev_comp": torch.cuda.Event(),
-                          "ev_out": torch.cuda.Event()})
         ncs = max(1, args.copy_streams)
         ups = [torch.cuda.Stream(dev) for _ in range(ncs)]
         downs = [torch.cuda.Stream(dev) for _ in range(ncs)]
@@ -477,7 +464,6 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                 for i in range(cut):
                     pieces.append((d[i * step_rows:(i + 1) * step_rows],
                                    s_[i * step_rows:(i + 1) * step_rows]) if cut > 1 else (d, s_))
-            evs = []
             for j, (d, s_) in enumerate(pieces):
                 st = streams[j % len(streams)]
                 with torch.cuda.stream(st):
@@ -489,45 +475,69 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                 streams[0].wait_event(e)
             done_ev.record(streams[0])
 
-        def e2e_step(k):
-            sl = slots[k % 2]
-            xd, wd, yd = sl["in"]
-            # step k-2 no longer reads these inputs once its fused call is done
-            split_copy((xd, wd, yd), (Xp, Wp, yp), ups, sl["ev_comp"], sl["ev_in"])
-            stream.wait_event(sl["ev_in"])
-            stream.wait_event(sl["ev_out"])         # step k-2's outputs are downloaded
-            lo, ls, dx, dw = sl["out"]
-            B.flce_fwd_bwd(xd, wd, yd, spec.ignore_index, spec.smoothing, spec.reduction,
-                           loss=lo, lse=ls, valid_count=sl["nv"], dX=dx, dW=dw,
-                           workspace_buf=ws, err_word=err, stream=stream, z_loss=args.z_loss,
-                           skip_ignored_blocks=args.skip_ignored, grad_filter=args.grad_filter)
-            sl["ev_comp"].record(stream)
-            split_copy(sl["host"], sl["out"], downs, sl["ev_comp"], sl["ev_out"])
+        def e2e_loop(read_all):
+            slots = []
+            for b in range(2):
+                if b == 0:
+                    dev_in = (X, W, y)
+                    dev_out = (loss, lse, dX, dW)
+                else:
+                    dev_in = (torch.empty_like(X), torch.empty_like(W), torch.empty_like(y))
+                    dev_out = (torch.empty_like(loss), torch.empty_like(lse),
+                               torch.empty_like(dX), torch.empty_like(dW))
+                read = dev_out if read_all else dev_out[:1]
+                host_out = tuple(torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in read)
+                slots.append({"in": dev_in, "out": dev_out, "read": read, "host": host_out,
+                              "nv": torch.empty_like(nv),
+                              "ev_in": torch.cuda.Event(), "ev_comp": torch.cuda.Event(),
+                              "ev_out": torch.cuda.Event()})
+            d2h = sum(t.numel() * t.element_size() for t in slots[0]["read"])
 
-        for k in range(max(args.warmup, 2)):
-            e2e_step(k)
-        torch.cuda.synchronize(dev)
-        if world > 1:
-            dist.barrier()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(s_up)
-        for k in range(args.steps):
-            e2e_step(k)
-        e1.record(s_down)
-        torch.cuda.synchronize(dev)
-        ems = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([ems], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
-        if int(err.item()) != 0:
-            raise RuntimeError(f"device error word {int(err.item())} in the end-to-end loop")
-        host_loss = float(slots[(args.steps - 1) % 2]["host"][0].item())
-        e2e = {"value": world * N * args.steps / (ems / 1e3), "unit": "tokens/s",
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "ms_per_step": ems / args.steps, "loss_read_back": host_loss,
-               "overlap": "uploads and downloads of neighbouring steps overlap the fused call",
-               "copy_streams_per_direction": ncs}
+            def e2e_step(k):
+                sl = slots[k % 2]
+                xd, wd, yd = sl["in"]
+                # step k-2 no longer reads these inputs once its fused call is done
+                split_copy((xd, wd, yd), (Xp, Wp, yp), ups, sl["ev_comp"], sl["ev_in"])
+                stream.wait_event(sl["ev_in"])
+                stream.wait_event(sl["ev_out"])         # step k-2's results are downloaded
+                lo, ls, dx, dw = sl["out"]
+                B.flce_fwd_bwd(xd, wd, yd, spec.ignore_index, spec.smoothing, spec.reduction,
+                               loss=lo, lse=ls, valid_count=sl["nv"], dX=dx, dW=dw,
+                               workspace_buf=ws, err_word=err, stream=stream,
+                               z_loss=args.z_loss, skip_ignored_blocks=args.skip_ignored,
+                               grad_filter=args.grad_filter)
+                sl["ev_comp"].record(stream)
+                split_copy(sl["host"], sl["read"], downs, sl["ev_comp"], sl["ev_out"])
+
+            for k in range(max(args.warmup, 2)):
+                e2e_step(k)
+            torch.cuda.synchronize(dev)
+            if world > 1:
+                dist.barrier()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s_up)
+            for k in range(args.steps):
+                e2e_step(k)
+            e1.record(s_down)
+            torch.cuda.synchronize(dev)
+            ems = e0.elapsed_time(e1)
+            if world > 1:
+                t = torch.tensor([ems], device=dev)
+                dist.all_reduce(t, op=dist.ReduceOp.MAX)
+                ems = float(t.item())
+            if int(err.item()) != 0:
+                raise RuntimeError(f"device error word {int(err.item())} in the end-to-end loop")
+            host_loss = float(slots[(args.steps - 1) % 2]["host"][0].item())
+            return {"value": world * N * args.steps / (ems / 1e3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                    "ms_per_step": ems / args.steps, "loss_read_back": host_loss,
+                    "read_back": "loss, lse, dX, dW" if read_all else "loss",
+                    "overlap": "uploads and downloads of neighbouring steps overlap the fused "
+                               "call",
+                    "copy_streams_per_direction": ncs}
+
+        e2e = e2e_loop(False)
+        e2e_all = e2e_loop(True)
 
     if rank != 0:
         return
@@ -620,6 +630,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "kernels": kinds,
         "cpu_baseline": cpu,
         "e2e": e2e,
+        "e2e_all_outputs": e2e_all,
         "gpu_launches": launches,
         "clocks": clocks,
         "wall_s_timed": wall,
