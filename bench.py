@@ -69,6 +69,8 @@ def parse_args():
                     help="z-loss weight alpha (adds alpha * lse^2 per valid token)")
     ap.add_argument("--single-cta", action="store_true",
                     help="128x256 single-CTA tiles instead of 256x256 CTA-pair tiles")
+    ap.add_argument("--clocks-dir", default=None,
+                    help="directory for the raw nvidia-smi clock samples (default: temp dir)")
     ap.add_argument("--merge", action="store_true",
                     help="one merged dW(c) + dX(c) + dZ(c+1) backward launch per vocabulary "
                          "chunk (two dZ buffers) instead of three launches")
@@ -179,9 +181,11 @@ CLOCK_FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slow
 
 
 class ClockSampler:
-    def __init__(self, gpu_index: str):
+    def __init__(self, gpu_index: str, out_dir: str | None = None):
+        import tempfile
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+        self.path = os.path.join(out_dir or tempfile.gettempdir(),
+                                 f"clocks_bench_{os.getpid()}.csv")
         try:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.fh = open(self.path, "w")
@@ -407,7 +411,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         if os.environ.get("CUDA_VISIBLE_DEVICES") else str(local_rank)
     B.flce_profile_reset()
     B.flce_profile_enable(True)
-    sampler = ClockSampler(gpu_index) if rank == 0 else None
+    sampler = ClockSampler(gpu_index, args.clocks_dir) if rank == 0 else None
     time.sleep(0.2 if sampler else 0.0)
     if world > 1:
         dist.barrier()

@@ -154,7 +154,9 @@ flce_status flce_fwd_bwd(const void* X, const void* W, const int64_t* labels, in
                          int accumulate_dW, void* workspace, size_t ws_bytes, int32_t* err_word,
                          void* stream);
 
-/* Options of the extended entry points.  Initialise with
+/* Options of the extended entry points: z-loss, a per-token loss output and
+ * skipping of fully ignored token blocks (instruction tuning), besides the
+ * options of the plain calls.  Initialise with
  * flce_options_init, then set fields:
  *   ignore_index  labels equal to it are masked (default -100)
  *   smoothing     label smoothing eps in [0, 1) (default 0)
@@ -215,7 +217,7 @@ flce_status flce_fwd_bwd_ex(const void* X, const void* W, const int64_t* labels,
                             int32_t* valid_count, void* dX, float* dW, int accumulate_dW,
                             void* workspace, size_t ws_bytes, int32_t* err_word, void* stream);
 
-/* Vocabulary-parallel layout (SURVEY row f3; the "tiled vocabulary dot
+/* Vocabulary-parallel layout (the "tiled vocabulary dot
  * products" of "Chunked and Fused Cross-Entropy ...", comparison table, with
  * step 2's running (m, d) carried across vocabulary shards).  Shard p holds
  * rows [vocab_offset, vocab_offset + V_shard) of W for a vocabulary of

@@ -157,3 +157,18 @@ def test_merged_parity_with_oracle():
     assert np.max(np.abs(got["lse"].double().numpy() - f.lse)) <= LSE_ABS
     assert rel_fro(got["dX"].double().numpy(), b.dX) <= GRAD_REL_FRO
     assert rel_fro(got["dW"].double().numpy(), b.dW) <= GRAD_REL_FRO
+
+
+@pytest.mark.slow
+def test_merged_equals_separate_launches_full_size():
+    """At the Llama-3 benchmark shape (N=8192, H=4096, V=128256) and Cv = 4096,
+    where merging pays: 32 merged launches of up to 1280 tiles, most of them round
+    robin, the last rounds handed out dynamically; same bits as three
+    launches per chunk."""
+    import torch
+    wl = I.make_workload(I.CONFIGS["llama3_n8192"], seed=0)
+    a, pa = _run(wl, True, 4096)
+    b, pb = _run(wl, False, 4096)
+    assert pa["bwd_merged"][1] == 32 and pb["bwd_dw_gemm"][1] == 32
+    for k in ("loss", "lse", "nv", "dX", "dW"):
+        assert torch.equal(a[k], b[k]), k
