@@ -62,6 +62,9 @@ CASES = [
     # dynamically handed-out last rounds
     (4096, 1024, 20000, 0, 0.0, 0.0, 4096, "bf16", 39),
     (6000, 1024, 16000, 100, 0.1, 1e-4, 2048, "bf16", 40),
+    # degenerate: one chunk (a merged launch with no dZ tiles), one token
+    (300, 128, 200, 20, 0.1, 0.0, 256, "bf16", 42),
+    (1, 64, 1000, 0, 0.0, 0.0, 256, "bf16", 43),
 ]
 
 
