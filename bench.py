@@ -295,7 +295,7 @@ def kind_flops(B, N, H, V, args, merged):
     out = {"fwd_logits_lse": full, "bwd_dz_recompute": full, "bwd_dw_gemm": full,
            "bwd_dx_gemm": full, "bwd_merged": 0.0}
     if merged:
-        dz0 = sum(2.0 * N * min(B.flce_vocab_chunk(N, v), v) * H for v in calls)
+        dz0 = sum(2.0 * N * min(B.flce_vocab_chunk(N, H, v), v) * H for v in calls)
         out["bwd_dz_recompute"] = dz0
         out["bwd_merged"] = 3.0 * full - dz0
     return out
@@ -342,7 +342,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     B.flce_set_l2_hints(args.l2_hints)
     B.flce_set_cta_pair(not args.single_cta)
     B.flce_set_backward_merge(args.merge)
-    chunk = B.flce_vocab_chunk(N, V)
+    chunk = B.flce_vocab_chunk(N, H, V)
 
     def host_tensor(a):
         if spec.dtype == "bf16":

@@ -86,11 +86,16 @@ size_t flce_workspace_size(int64_t N, int64_t H, int64_t V, flce_dtype dtype, in
 /* Vocabulary columns per backward chunk (Cv): the gradient scratch is N x Cv
  * bf16, two such buffers when the merged backward below is enabled.  0 (the
  * default) picks the largest multiple of 256 whose buffers together fit in
- * 256 MiB; a default or set value is rounded up to a multiple of 256 and
- * clamped to [256, V/2] (one buffer) or [256, V/4] (two buffers).
- * Process-wide; set it before sizing workspaces. */
+ * 256 MiB, clamped to [256, V/2] (one buffer) or [256, V/4] (two buffers);
+ * with one buffer it is then rounded down to a width whose weight-gradient
+ * launch is a whole number of waves of the current device's CTA pairs
+ * ((Cv / 256) * ceil(H / 256) a multiple of the pair count) when that keeps at
+ * least 7/8 of it.  A set value is rounded up to a multiple of 256 and
+ * clamped the same way.  Process-wide; set it before sizing workspaces.
+ * flce_vocab_chunk returns the width a call of this shape uses (0 on invalid
+ * arguments). */
 flce_status flce_set_vocab_chunk(int64_t cols);
-int64_t flce_vocab_chunk(int64_t N, int64_t V);
+int64_t flce_vocab_chunk(int64_t N, int64_t H, int64_t V);
 
 /* GEMM tile shape, process-wide.  1 (the default): a cluster of two CTAs on
  * two SMs computes each 256 x 256 tile with tcgen05.mma.cta_group::2, each CTA

@@ -80,7 +80,7 @@ def lib() -> ctypes.CDLL:
     L.flce_workspace_size.restype = SZ
     L.flce_set_vocab_chunk.argtypes = [I64]
     L.flce_set_vocab_chunk.restype = I32
-    L.flce_vocab_chunk.argtypes = [I64, I64]
+    L.flce_vocab_chunk.argtypes = [I64, I64, I64]
     L.flce_vocab_chunk.restype = I64
     L.flce_forward.argtypes = [P, P, P, I64, I64, I64, I64, F32, I32, I32, P, P, P, P, SZ, P, P]
     L.flce_forward.restype = I32
@@ -224,8 +224,8 @@ def flce_backward_merge() -> bool:
     return bool(lib().flce_backward_merge())
 
 
-def flce_vocab_chunk(N: int, V: int) -> int:
-    return int(lib().flce_vocab_chunk(N, V))
+def flce_vocab_chunk(N: int, H: int, V: int) -> int:
+    return int(lib().flce_vocab_chunk(N, H, V))
 
 
 def workspace(N: int, H: int, V: int, dtype: int, mode: int, device) -> torch.Tensor:

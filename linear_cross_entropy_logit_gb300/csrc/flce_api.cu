@@ -27,6 +27,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <numeric>
 #include <string>
 #include <vector>
 
@@ -124,18 +125,41 @@ bool shape_ok(int64_t N, int64_t H, int64_t V) {
 bool merge_planned() { return g_bwd_merge.load() != 0 && g_cta_pair.load() != 0; }
 int dz_buffers() { return merge_planned() ? 2 : 1; }
 
+// CTA pairs of a persistent launch on the current device (76 on a 152-SM
+// GB300, also the value when no device can be queried).
+int64_t device_pairs() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+      sms >= 2)
+    return sms / 2;
+  (void)cudaGetLastError();  // clear the failed query's error
+  return 76;
+}
+
+// Three-launch backward: the dW launch of a chunk has (Cv / 256) x ceil(H / 256)
+// tiles; when that is a whole number of waves of CTA pairs no launch ends on a
+// partial wave.  The width is rounded down to such a multiple when that keeps
+// at least 7/8 of it (Llama-3 shape: 16384 -> 14592, 12 waves; measured 2.6%
+// faster dW launches and slightly faster steps on a GB300).
+int64_t wave_aligned(int64_t c, int64_t H) {
+  const int64_t pairs = device_pairs();
+  const int64_t hb = ceil_div(H, BN);
+  const int64_t step = 256 * (pairs / std::gcd(hb, pairs));
+  const int64_t a = c / step * step;
+  return (a >= 256 && a * 8 >= c * 7) ? a : c;
+}
+
 // Cv: the dZ buffers together take at most kDzBudget (default) and at most
-// half of the N x V logits (each buffer at most V / (2 * buffers) columns).
-int64_t auto_chunk(int64_t N, int64_t V) {
+// half of the N x V logits (each buffer at most V / (2 * buffers) columns); the
+// default width is wave-aligned for the three-launch backward.
+int64_t auto_chunk(int64_t N, int64_t H, int64_t V) {
   const int64_t half = std::max<int64_t>(256, (V / (2 * dz_buffers())) / 256 * 256);
   int64_t set = g_vocab_chunk.load();
-  int64_t c;
-  if (set > 0) {
-    c = ceil_div(set, 256) * 256;
-  } else {
-    c = (kDzBudget / dz_buffers() / (std::max<int64_t>(N, 1) * 2)) / 256 * 256;
-  }
-  return std::min(std::max<int64_t>(c, 256), half);
+  if (set > 0) return std::min(std::max<int64_t>(ceil_div(set, 256) * 256, 256), half);
+  int64_t c = (kDzBudget / dz_buffers() / (std::max<int64_t>(N, 1) * 2)) / 256 * 256;
+  c = std::min(std::max<int64_t>(c, 256), half);
+  return merge_planned() ? c : wave_aligned(c, H);
 }
 
 bool make_plan(int64_t N, int64_t H, int64_t V, flce_dtype dtype, int mode, Plan* pl) {
@@ -154,7 +178,7 @@ bool make_plan(int64_t N, int64_t H, int64_t V, flce_dtype dtype, int mode, Plan
   p.group_len = L;
   p.n_groups = (int)ceil_div(p.v_tiles, L);
   p.merge_blocks = (int)ceil_div(std::max<int64_t>(N, 1), MERGE_THREADS);
-  p.chunk = auto_chunk(N, V);
+  p.chunk = auto_chunk(N, H, V);
   p.n_chunks = (int)ceil_div(V, p.chunk);
   p.dz_bufs = dz_buffers();
   const bool fwd = mode & FLCE_MODE_FWD;
@@ -865,7 +889,7 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
 // ===========================================================================
 extern "C" {
 
-int flce_abi_version(void) { return 104; }
+int flce_abi_version(void) { return 105; }
 
 const char* flce_status_string(flce_status s) {
   switch (s) {
@@ -943,9 +967,9 @@ flce_status flce_set_vocab_chunk(int64_t cols) {
   return FLCE_OK;
 }
 
-int64_t flce_vocab_chunk(int64_t N, int64_t V) {
-  if (N < 0 || V <= 0) return 0;
-  return auto_chunk(N, V);
+int64_t flce_vocab_chunk(int64_t N, int64_t H, int64_t V) {
+  if (N < 0 || H <= 0 || V <= 0) return 0;
+  return auto_chunk(N, H, V);
 }
 
 size_t flce_workspace_size(int64_t N, int64_t H, int64_t V, flce_dtype dtype, int mode) {

@@ -35,7 +35,7 @@ def _run(wl, merge, chunk, reduction="mean", grad=None, dW0=None, z_loss=0.0):
     from linear_cross_entropy_logit_gb300 import binding as B
     B.flce_set_backward_merge(merge)
     B.flce_set_vocab_chunk(chunk)
-    assert B.flce_vocab_chunk(wl.N, wl.spec.V) == chunk  # same Cv on both paths
+    assert B.flce_vocab_chunk(wl.N, wl.spec.H, wl.spec.V) == chunk  # same Cv on both paths
     X, W, y = to_device(wl)
     g = None if grad is None else torch.tensor([grad], dtype=torch.float32, device="cuda")
     dW = None if dW0 is None else torch.from_numpy(dW0).cuda()
@@ -116,7 +116,7 @@ def test_merged_vocab_shard_backward():
     for merge in (True, False):
         B.flce_set_backward_merge(merge)
         B.flce_set_vocab_chunk(512)
-        assert B.flce_vocab_chunk(500, 2200) == 512
+        assert B.flce_vocab_chunk(500, 256, 2200) == 512
         dxp, dwp, e = B.flce_backward_vocab_shard(X, W[1800:], y, 1800, 4000, lse, nv, opt)
         torch.cuda.synchronize()
         assert int(e.item()) == 0

@@ -41,7 +41,7 @@ def test_header_exports_all(L):
 
 
 def test_status_strings_and_version(L):
-    assert L.flce_abi_version() == 104
+    assert L.flce_abi_version() == 105
     for s in range(7):
         assert L.flce_status_string(s).decode().startswith("FLCE_")
 
@@ -54,7 +54,7 @@ def test_workspace_plan_bounded():
         if spec.dtype != "bf16":
             continue
         N, H, V = spec.N, spec.H, spec.V
-        cv = B.flce_vocab_chunk(N, V)
+        cv = B.flce_vocab_chunk(N, H, V)
         bufs = _dz_buffers(B)
         assert cv % 256 == 0 and 256 <= cv <= V // (2 * bufs)
         nxv = N * V * 2
@@ -75,7 +75,7 @@ def test_workspace_matches_pages_fused_figure():
     figs = json.load(open(os.path.join(ROOT, "tests", "golden", "pages_memory_figures.json")))
     fused = [f for f in figs["figures"] if f["N"] == 1024 and f["V"] == 128256][0]
     B.flce_set_vocab_chunk(0)
-    cv = B.flce_vocab_chunk(8192, 128256)
+    cv = B.flce_vocab_chunk(8192, 4096, 128256)
     assert _dz_buffers(B) * 8192 * cv * 2 / 1e9 <= fused["printed_gb"] + 0.01
 
 
@@ -97,15 +97,16 @@ def test_backward_merge_setting():
     B.flce_set_vocab_chunk(0)
     try:
         B.flce_set_backward_merge(True)
-        cv2 = B.flce_vocab_chunk(N, V)
+        cv2 = B.flce_vocab_chunk(N, H, V)
         ws2 = B.flce_workspace_size(N, H, V, B.FLCE_BF16, B.MODE_BWD)
         B.flce_set_backward_merge(False)
-        cv1 = B.flce_vocab_chunk(N, V)
+        cv1 = B.flce_vocab_chunk(N, H, V)
         ws1 = B.flce_workspace_size(N, H, V, B.FLCE_BF16, B.MODE_BWD)
-        assert (cv1, cv2) == (16384, 8192)
-        # same dZ bytes; only the tile counters and the filter masks (sized
-        # by Cv) differ
-        assert abs(ws2 - ws1) <= 64 << 10
+        # two buffers of half the budget; one wave-aligned buffer (16384 -> 14592)
+        assert (cv1, cv2) == (14592, 8192)
+        # the dZ bytes differ by the buffers; the tile counters and the filter
+        # masks (sized by Cv) by a few KiB
+        assert abs((ws2 - ws1) - N * 2 * (2 * cv2 - cv1)) <= 64 << 10
         B.flce_set_vocab_chunk(2048)
         a = B.flce_workspace_size(N, H, V, B.FLCE_BF16, B.MODE_BWD)
         B.flce_set_backward_merge(True)
@@ -116,14 +117,40 @@ def test_backward_merge_setting():
         B.flce_set_vocab_chunk(0)
 
 
+def test_default_chunk_is_wave_aligned_when_close():
+    """With one dZ buffer the default width is rounded down to a multiple of
+    256 * P / gcd(ceil(H/256), P) (P = 76 CTA pairs on a 152-SM GB300, also the
+    value without a device) when that keeps at least 7/8 of the budget width,
+    so the dW launch (Cv/256 x H/256 tiles) is whole waves."""
+    import math
+    from linear_cross_entropy_logit_gb300 import binding as B
+    B.flce_set_vocab_chunk(0)
+    assert not B.flce_backward_merge()
+    P = 76
+    cases = {  # (N, H, V): (budget width, expected)
+        (8192, 4096, 128256): (16384, 14592),   # 57 blocks x 16 = 912 tiles = 12 waves
+        (16384, 4096, 128256): (8192, 8192),    # 4864 would keep only 59%
+        (16384, 3584, 152064): (8192, 8192),    # the aligned step (9728) exceeds the budget
+        (32768, 2304, 256000): (4096, 4096),    # step 19456
+    }
+    for (N, H, V), (budget, want) in cases.items():
+        cv = B.flce_vocab_chunk(N, H, V)
+        assert cv == want, (N, H, V, cv)
+        hb = -(-H // 256)
+        step = 256 * (P // math.gcd(hb, P))
+        assert cv == budget or (cv % step == 0 and cv * 8 >= budget * 7)
+        if cv != budget:
+            assert (cv // 256) * hb % P == 0
+
+
 def test_vocab_chunk_setting():
     from linear_cross_entropy_logit_gb300 import binding as B
     try:
         B.flce_set_vocab_chunk(1000)
-        assert B.flce_vocab_chunk(8192, 128256) == 1024
+        assert B.flce_vocab_chunk(8192, 4096, 128256) == 1024
         B.flce_set_vocab_chunk(10 ** 9)
         bufs = _dz_buffers(B)
-        assert B.flce_vocab_chunk(8192, 128256) == 128256 // (2 * bufs) // 256 * 256
+        assert B.flce_vocab_chunk(8192, 4096, 128256) == 128256 // (2 * bufs) // 256 * 256
     finally:
         B.flce_set_vocab_chunk(0)
 
