@@ -197,3 +197,40 @@ def test_options_struct_layout(L):
     st = L.flce_forward_ex(P(fake), P(fake), P(fake), 4, 16, 16, 0, ctypes.byref(o), P(fake),
                            P(fake), P(fake), P(fake), 1 << 20, P(fake), None)
     assert st == B.FLCE_ERR_ARG
+
+
+def test_plain_c_caller(L, tmp_path):
+    """include/flce.h is a C header: a C99 program compiles against it with
+    -pedantic, links against libflce.so and gets the same answers as the
+    Python binding from the host-only entry points."""
+    import shutil
+    import subprocess
+    from linear_cross_entropy_logit_gb300 import binding as B
+    from linear_cross_entropy_logit_gb300 import build as libbuild
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "caller.c"
+    src.write_text(
+        '#include <stdio.h>\n'
+        '#include "flce.h"\n'
+        'int main(void) {\n'
+        '  flce_options o;\n'
+        '  flce_options_init(&o);\n'
+        '  printf("%d %lld %zu %lld %s\\n", flce_abi_version(), (long long)o.ignore_index,\n'
+        '         flce_workspace_size(8192, 4096, 128256, FLCE_BF16, FLCE_MODE_FWD_BWD),\n'
+        '         (long long)flce_vocab_chunk(8192, 4096, 128256),\n'
+        '         flce_status_string(FLCE_ERR_ARG));\n'
+        '  return 0;\n'
+        '}\n')
+    exe = tmp_path / "caller"
+    libdir = os.path.dirname(libbuild.LIB)
+    subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I",
+                    os.path.join(ROOT, "include"), str(src), "-L", libdir, "-lflce",
+                    f"-Wl,-rpath,{libdir}", "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()
+    assert int(out[0]) == L.flce_abi_version()
+    assert int(out[1]) == -100
+    assert int(out[2]) == B.flce_workspace_size(8192, 4096, 128256, B.FLCE_BF16, B.MODE_FWD_BWD)
+    assert int(out[3]) == B.flce_vocab_chunk(8192, 4096, 128256)
+    assert out[4].startswith("FLCE_ERR_ARG")
