@@ -71,7 +71,9 @@ typedef enum {
   FLCE_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required  */
   FLCE_ERR_LABEL = 4,        /* (err_word only) label outside [0, V)        */
   FLCE_ERR_TIMEOUT = 5,      /* (err_word only) a bounded device wait expired */
-  FLCE_ERR_CUDA = 6          /* a CUDA runtime/driver call failed           */
+  FLCE_ERR_CUDA = 6,         /* a CUDA runtime/driver call failed           */
+  FLCE_ERR_BOUNDS = 7        /* (err_word only, debug build) an index check
+                                failed; the access was skipped              */
 } flce_status;
 
 typedef enum { FLCE_BF16 = 0, FLCE_FP32 = 1 } flce_dtype;
@@ -80,7 +82,12 @@ typedef enum { FLCE_MODE_FWD = 1, FLCE_MODE_BWD = 2, FLCE_MODE_FWD_BWD = 3 } flc
 
 /* Bytes of workspace one call of `mode` needs for this shape (0 on invalid
  * arguments).  Pure host arithmetic: needs no GPU.  The layout depends only on
- * (N, H, V, dtype, mode) and the vocabulary chunk setting below. */
+ * (N, H, V, dtype, mode) and the launch settings -- the vocabulary chunk
+ * width, merged backward launches and the tile shape.  This form reads the
+ * process-wide settings below at the time of the call; flce_workspace_size_ex
+ * (after flce_options) takes them from an options struct, so that sizing and
+ * the call that uses the workspace cannot disagree when another thread changes
+ * a process-wide setting in between. */
 size_t flce_workspace_size(int64_t N, int64_t H, int64_t V, flce_dtype dtype, int mode);
 
 /* Vocabulary columns per backward chunk (Cv): the gradient scratch is N x Cv
@@ -91,20 +98,23 @@ size_t flce_workspace_size(int64_t N, int64_t H, int64_t V, flce_dtype dtype, in
  * launch is a whole number of waves of the current device's CTA pairs
  * ((Cv / 256) * ceil(H / 256) a multiple of the pair count) when that keeps at
  * least 7/8 of it.  A set value is rounded up to a multiple of 256 and
- * clamped the same way.  Process-wide; set it before sizing workspaces.
- * flce_vocab_chunk returns the width a call of this shape uses (0 on invalid
- * arguments). */
+ * clamped the same way.  Process-wide default of the calls whose options leave
+ * vocab_chunk at -1 (the plain calls always use it); set it before sizing
+ * workspaces.  flce_vocab_chunk returns the width such a call of this shape
+ * uses (0 on invalid arguments). */
 flce_status flce_set_vocab_chunk(int64_t cols);
 int64_t flce_vocab_chunk(int64_t N, int64_t H, int64_t V);
 
-/* GEMM tile shape, process-wide.  1 (the default): a cluster of two CTAs on
- * two SMs computes each 256 x 256 tile with tcgen05.mma.cta_group::2, each CTA
- * loading its own 128 rows of A and half of B.  0: one CTA per 128 x 256 tile.
- * Both give the same results up to fp32 summation order. */
+/* GEMM tile shape, process-wide default (options field cta_pair overrides it
+ * per call).  1 (the default): a cluster of two CTAs on two SMs computes each
+ * 256 x 256 tile with tcgen05.mma.cta_group::2, each CTA loading its own 128
+ * rows of A and half of B.  0: one CTA per 128 x 256 tile.  Both give the
+ * same results up to fp32 summation order. */
 flce_status flce_set_cta_pair(int on);
 int flce_cta_pair(void);
 
-/* Merged backward launches, process-wide.  1: with CTA-pair tiles and none of
+/* Merged backward launches, process-wide default (options field
+ * backward_merge overrides it per call).  1: with CTA-pair tiles and none of
  * the optional features (skip_ignored_blocks, grad_filter, L2 hints), the
  * backward runs the dZ recompute of chunk 0 alone and then one launch per
  * vocabulary chunk c holding the dW and dX GEMMs of c and the dZ recompute of
@@ -119,7 +129,8 @@ int flce_cta_pair(void);
 flce_status flce_set_backward_merge(int on);
 int flce_backward_merge(void);
 
-/* L2 residency hints, process-wide.  1: the operand a GEMM re-reads on every
+/* L2 residency hints, process-wide default (options field l2_hints overrides
+ * it per call).  1: the operand a GEMM re-reads on every
  * wave of tiles (X, or a W chunk) is loaded with an evict_last policy covering
  * up to ~64 MB of L2.  0 (the default; on a GB300 the hints did not speed up
  * the llama3-shaped step and slowed the dW GEMM by ~3%): no hints.  Results do
@@ -191,7 +202,20 @@ flce_status flce_fwd_bwd(const void* X, const void* W, const int64_t* labels, in
  *                 |dZ| <= c * max((1 + 2 alpha lse) eps_f, eps / V), so
  *                 |delta dX|_F <= |delta dZ|_F |W|_2 and |delta dW|_F <=
  *                 |delta dZ|_F |X|_2.  Needs ceil(Cv/64) and ceil(N/64) <= 1024
- *                 (else FLCE_ERR_UNSUPPORTED); loss and lse are exact. */
+ *                 (else FLCE_ERR_UNSUPPORTED); loss and lse are exact.
+ * Launch settings of this call (ABI 1.06; flce_options_init sets each to -1,
+ * which takes the process-wide setting of the matching flce_set_* call at
+ * the time of the call; any other value holds for this call only, so callers
+ * in several threads can use different settings without racing):
+ *   cta_pair        -1, 0 or 1: see flce_set_cta_pair
+ *   backward_merge  -1, 0 or 1: see flce_set_backward_merge
+ *   l2_hints        -1, 0 or 1: see flce_set_l2_hints
+ *   vocab_chunk     -1, 0 (automatic width) or a width in columns: see
+ *                   flce_set_vocab_chunk
+ * The workspace of a call must be sized with the same settings:
+ * flce_workspace_size_ex with the same options.  A struct from a caller built
+ * against ABI 1.05 (struct_size = offsetof(flce_options, cta_pair)) is
+ * accepted and runs with the process-wide settings. */
 typedef struct flce_options {
   size_t struct_size;
   int64_t ignore_index;
@@ -201,9 +225,19 @@ typedef struct flce_options {
   float* row_loss;
   int skip_ignored_blocks;
   float grad_filter;
+  int cta_pair;
+  int backward_merge;
+  int l2_hints;
+  int64_t vocab_chunk;
 } flce_options;
 
 void flce_options_init(flce_options* opt);
+
+/* flce_workspace_size / flce_vocab_chunk for a call made with these options
+ * (NULL: the process-wide settings).  0 on invalid arguments or options. */
+size_t flce_workspace_size_ex(int64_t N, int64_t H, int64_t V, flce_dtype dtype, int mode,
+                              const flce_options* opt);
+int64_t flce_vocab_chunk_ex(int64_t N, int64_t H, int64_t V, const flce_options* opt);
 
 flce_status flce_forward_ex(const void* X, const void* W, const int64_t* labels, int64_t N,
                             int64_t H, int64_t V, flce_dtype dtype, const flce_options* opt,
@@ -237,9 +271,10 @@ flce_status flce_fwd_bwd_ex(const void* X, const void* W, const int64_t* labels,
  *      valid_count -> its fp32 partial dX (N x H; the shards' partials sum to
  *      dX: an all-reduce) and its own dW rows (V_shard x H fp32).
  * opt: ignore_index, smoothing (eps / vocab_total per class), z_loss,
- * reduction; row_loss only in the combine; skip_ignored_blocks must be 0.
- * Workspaces: flce_workspace_size(N, H, V_shard, dtype, FLCE_MODE_FWD / _BWD)
- * for the shard calls, flce_combine_workspace_size(N) for the combine. */
+ * reduction and the launch settings; row_loss only in the combine;
+ * skip_ignored_blocks must be 0.  Workspaces: flce_workspace_size_ex(N, H,
+ * V_shard, dtype, FLCE_MODE_FWD / _BWD, opt) for the shard calls,
+ * flce_combine_workspace_size(N) for the combine. */
 flce_status flce_forward_vocab_shard(const void* X, const void* W_shard, const int64_t* labels,
                                      int64_t N, int64_t H, int64_t V_shard, int64_t vocab_offset,
                                      int64_t vocab_total, flce_dtype dtype,
@@ -289,8 +324,14 @@ void flce_profile_reset(void);
  * that cannot call cudaMalloc or keep a workspace -- code inside a host
  * application that owns all device memory through its own fixed pool, code
  * on a path that must not allocate after start-up, and C callers without an
- * allocator.  Results equal flce_forward's (loss, lse, valid_count, err_word
- * as there); bf16 X and W only.
+ * allocator.  Outputs as flce_forward's (loss, lse, valid_count, err_word);
+ * the values match flce_forward's within the parity tolerances, not bit for
+ * bit: this entry point always runs the 128 x 256 single-CTA tiles with its
+ * own vocabulary grouping, so its sums run in another order.  bf16 X and W
+ * only.  err_word, loss, valid_count and lse must be 4-byte aligned.
+ * loss and lse are undefined whenever *err_word is FLCE_ERR_TIMEOUT after
+ * the call: the merge may then have read partials an earlier call left in
+ * the shared scratch.
  * Scratch: a fixed device array of FLCE_NOALLOC_SCRATCH_BYTES inside the
  * library, held on every GPU that runs this entry point until the process
  * exits.  The first call on a device looks up the array's address (make that

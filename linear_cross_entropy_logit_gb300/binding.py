@@ -14,6 +14,9 @@ import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_lib", "libflce.so")
+# The same library built with FLCE_DEBUG: index math range-checked on the
+# device (an out-of-range index sets FLCE_ERR_BOUNDS instead of being used).
+DEBUG_LIB_PATH = os.path.join(_HERE, "_lib", "libflce_debug.so")
 
 FLCE_OK = 0
 FLCE_ERR_ARG = 1
@@ -22,6 +25,7 @@ FLCE_ERR_WORKSPACE = 3
 FLCE_ERR_LABEL = 4
 FLCE_ERR_TIMEOUT = 5
 FLCE_ERR_CUDA = 6
+FLCE_ERR_BOUNDS = 7
 
 FLCE_BF16 = 0
 FLCE_FP32 = 1
@@ -40,6 +44,7 @@ EXPORTED = (
     "flce_forward_ex", "flce_backward_ex", "flce_fwd_bwd_ex", "flce_forward_vocab_shard",
     "flce_combine_workspace_size", "flce_combine_vocab_shards", "flce_backward_vocab_shard",
     "flce_debug_wait_timeout", "flce_set_backward_merge", "flce_backward_merge",
+    "flce_workspace_size_ex", "flce_vocab_chunk_ex",
 )
 
 PROFILE_KINDS = ("fwd_logits_lse", "bwd_dz_recompute", "bwd_dw_gemm", "bwd_dx_gemm",
@@ -53,7 +58,9 @@ class FlceOptions(ctypes.Structure):
     _fields_ = [("struct_size", ctypes.c_size_t), ("ignore_index", ctypes.c_int64),
                 ("smoothing", ctypes.c_float), ("z_loss", ctypes.c_float),
                 ("reduction", ctypes.c_int), ("row_loss", ctypes.c_void_p),
-                ("skip_ignored_blocks", ctypes.c_int), ("grad_filter", ctypes.c_float)]
+                ("skip_ignored_blocks", ctypes.c_int), ("grad_filter", ctypes.c_float),
+                ("cta_pair", ctypes.c_int), ("backward_merge", ctypes.c_int),
+                ("l2_hints", ctypes.c_int), ("vocab_chunk", ctypes.c_int64)]
 
 
 class FlceError(RuntimeError):
@@ -68,13 +75,27 @@ class FlceError(RuntimeError):
 def lib() -> ctypes.CDLL:
     """Load the library (once).  Raises if it has not been built."""
     global _lib
-    if _lib is not None:
-        return _lib
-    if not os.path.exists(LIB_PATH):
+    if _lib is None:
+        _lib = load(LIB_PATH)
+    return _lib
+
+
+def use_library(L: Optional[ctypes.CDLL]) -> Optional[ctypes.CDLL]:
+    """Make every wrapper below call ``L`` (e.g. ``load(DEBUG_LIB_PATH)``);
+    returns the library used before.  ``None`` goes back to the default."""
+    global _lib
+    prev = _lib
+    _lib = L
+    return prev
+
+
+def load(path: str) -> ctypes.CDLL:
+    """Open a build of the library and declare its C signatures."""
+    if not os.path.exists(path):
         raise RuntimeError(
-            f"{LIB_PATH} is missing: build it with "
+            f"{path} is missing: build it with "
             "`python -m linear_cross_entropy_logit_gb300.build` (needs nvcc)")
-    L = ctypes.CDLL(LIB_PATH)
+    L = ctypes.CDLL(path)
     P, I64, I32, F32, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     L.flce_workspace_size.argtypes = [I64, I64, I64, I32, I32]
     L.flce_workspace_size.restype = SZ
@@ -143,7 +164,10 @@ def lib() -> ctypes.CDLL:
     L.flce_backward_vocab_shard.restype = I32
     L.flce_debug_wait_timeout.argtypes = [P, ctypes.c_uint64, P, P]
     L.flce_debug_wait_timeout.restype = I32
-    _lib = L
+    L.flce_workspace_size_ex.argtypes = [I64, I64, I64, I32, I32, OPT]
+    L.flce_workspace_size_ex.restype = SZ
+    L.flce_vocab_chunk_ex.argtypes = [I64, I64, I64, OPT]
+    L.flce_vocab_chunk_ex.restype = I64
     return L
 
 
@@ -193,8 +217,13 @@ def _check_inputs(X, W, labels):
     return N, H, V
 
 
-def flce_workspace_size(N: int, H: int, V: int, dtype: int = FLCE_BF16, mode: int = MODE_FWD_BWD) -> int:
-    return int(lib().flce_workspace_size(N, H, V, dtype, mode))
+def flce_workspace_size(N: int, H: int, V: int, dtype: int = FLCE_BF16, mode: int = MODE_FWD_BWD,
+                        options: Optional["FlceOptions"] = None) -> int:
+    """Workspace bytes; with ``options`` the launch settings are taken from them
+    (flce_workspace_size_ex), else from the process-wide defaults."""
+    if options is None:
+        return int(lib().flce_workspace_size(N, H, V, dtype, mode))
+    return int(lib().flce_workspace_size_ex(N, H, V, dtype, mode, ctypes.byref(options)))
 
 
 def flce_set_vocab_chunk(cols: int) -> None:
@@ -224,14 +253,19 @@ def flce_backward_merge() -> bool:
     return bool(lib().flce_backward_merge())
 
 
-def flce_vocab_chunk(N: int, H: int, V: int) -> int:
-    return int(lib().flce_vocab_chunk(N, H, V))
+def flce_vocab_chunk(N: int, H: int, V: int, options: Optional["FlceOptions"] = None) -> int:
+    if options is None:
+        return int(lib().flce_vocab_chunk(N, H, V))
+    return int(lib().flce_vocab_chunk_ex(N, H, V, ctypes.byref(options)))
 
 
-def workspace(N: int, H: int, V: int, dtype: int, mode: int, device) -> torch.Tensor:
+def workspace(N: int, H: int, V: int, dtype: int, mode: int, device,
+              options: Optional["FlceOptions"] = None) -> torch.Tensor:
     """A workspace of the required size (torch-allocated, 256-byte aligned)."""
-    n = max(flce_workspace_size(N, H, V, dtype, mode), 256)
-    return torch.empty(n, dtype=torch.uint8, device=device)
+    n = flce_workspace_size(N, H, V, dtype, mode, options)
+    if n == 0:
+        raise ValueError(f"no workspace plan for N={N}, H={H}, V={V} with these options")
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
 
 
 def new_err_word(device) -> torch.Tensor:
@@ -240,7 +274,11 @@ def new_err_word(device) -> torch.Tensor:
 
 def make_options(ignore_index: int = -100, smoothing: float = 0.0, reduction: str = "mean",
                  z_loss: float = 0.0, row_loss=None, skip_ignored_blocks: bool = False,
-                 grad_filter: float = 0.0) -> FlceOptions:
+                 grad_filter: float = 0.0, *, cta_pair: Optional[bool] = None,
+                 backward_merge: Optional[bool] = None, l2_hints: Optional[bool] = None,
+                 vocab_chunk: Optional[int] = None) -> FlceOptions:
+    """An ``flce_options``; the launch settings left at None take the
+    process-wide defaults at the time of each call."""
     o = FlceOptions()
     lib().flce_options_init(ctypes.byref(o))
     o.ignore_index = ignore_index
@@ -250,6 +288,14 @@ def make_options(ignore_index: int = -100, smoothing: float = 0.0, reduction: st
     o.row_loss = _ptr(row_loss)
     o.skip_ignored_blocks = int(bool(skip_ignored_blocks))
     o.grad_filter = grad_filter
+    if cta_pair is not None:
+        o.cta_pair = int(bool(cta_pair))
+    if backward_merge is not None:
+        o.backward_merge = int(bool(backward_merge))
+    if l2_hints is not None:
+        o.l2_hints = int(bool(l2_hints))
+    if vocab_chunk is not None:
+        o.vocab_chunk = int(vocab_chunk)
     return o
 
 
@@ -287,7 +333,7 @@ def flce_forward_ex(X, W, labels, options: FlceOptions, *, loss=None, lse=None,
     loss = torch.empty(1, dtype=torch.float32, device=dev) if loss is None else loss
     lse = torch.empty(N, dtype=torch.float32, device=dev) if lse is None else lse
     valid_count = torch.empty(1, dtype=torch.int32, device=dev) if valid_count is None else valid_count
-    ws = workspace(N, H, V, dt, MODE_FWD, dev) if workspace_buf is None else workspace_buf
+    ws = workspace(N, H, V, dt, MODE_FWD, dev, options) if workspace_buf is None else workspace_buf
     err_word = new_err_word(dev) if err_word is None else err_word
     st = lib().flce_forward_ex(_ptr(X), _ptr(W), _ptr(labels), N, H, V, dt, ctypes.byref(options),
                                _ptr(loss), _ptr(lse), _ptr(valid_count), _ptr(ws), ws.numel(),
@@ -339,7 +385,7 @@ def flce_backward_ex(X, W, labels, lse, valid_count, options: FlceOptions, *, gr
         if accumulate_dW:
             raise ValueError("accumulate_dW needs an existing dW")
         dW = torch.empty(V, H, dtype=torch.float32, device=dev)
-    ws = workspace(N, H, V, dt, MODE_BWD, dev) if workspace_buf is None else workspace_buf
+    ws = workspace(N, H, V, dt, MODE_BWD, dev, options) if workspace_buf is None else workspace_buf
     err_word = new_err_word(dev) if err_word is None else err_word
     st = lib().flce_backward_ex(_ptr(X), _ptr(W), _ptr(labels), N, H, V, dt,
                                 ctypes.byref(options), _ptr(lse), _ptr(valid_count),
@@ -398,7 +444,7 @@ def flce_fwd_bwd_ex(X, W, labels, options: FlceOptions, *, grad_loss=None, loss=
         if accumulate_dW:
             raise ValueError("accumulate_dW needs an existing dW")
         dW = torch.empty(V, H, dtype=torch.float32, device=dev)
-    ws = workspace(N, H, V, dt, MODE_FWD_BWD, dev) if workspace_buf is None else workspace_buf
+    ws = workspace(N, H, V, dt, MODE_FWD_BWD, dev, options) if workspace_buf is None else workspace_buf
     err_word = new_err_word(dev) if err_word is None else err_word
     st = lib().flce_fwd_bwd_ex(_ptr(X), _ptr(W), _ptr(labels), N, H, V, dt, ctypes.byref(options),
                                _ptr(grad_loss), _ptr(loss), _ptr(lse), _ptr(valid_count),
@@ -417,7 +463,7 @@ def flce_forward_vocab_shard(X, W_shard, labels, vocab_offset: int, vocab_total:
     dt = _dtype_code(X)
     options = make_options() if options is None else options
     partials = torch.empty(N, 4, dtype=torch.float32, device=dev) if partials is None else partials
-    ws = workspace(N, H, Vs, dt, MODE_FWD, dev) if workspace_buf is None else workspace_buf
+    ws = workspace(N, H, Vs, dt, MODE_FWD, dev, options) if workspace_buf is None else workspace_buf
     err_word = new_err_word(dev) if err_word is None else err_word
     st = lib().flce_forward_vocab_shard(_ptr(X), _ptr(W_shard), _ptr(labels), N, H, Vs,
                                         vocab_offset, vocab_total, dt, ctypes.byref(options),
@@ -458,7 +504,7 @@ def flce_backward_vocab_shard(X, W_shard, labels, vocab_offset: int, vocab_total
     options = make_options() if options is None else options
     dX_partial = torch.empty(N, H, dtype=torch.float32, device=dev) if dX_partial is None else dX_partial
     dW_shard = torch.empty(Vs, H, dtype=torch.float32, device=dev) if dW_shard is None else dW_shard
-    ws = workspace(N, H, Vs, dt, MODE_BWD, dev) if workspace_buf is None else workspace_buf
+    ws = workspace(N, H, Vs, dt, MODE_BWD, dev, options) if workspace_buf is None else workspace_buf
     err_word = new_err_word(dev) if err_word is None else err_word
     st = lib().flce_backward_vocab_shard(_ptr(X), _ptr(W_shard), _ptr(labels), N, H, Vs,
                                          vocab_offset, vocab_total, dt, ctypes.byref(options),

@@ -100,7 +100,8 @@ __device__ __forceinline__ FusedTile fused_tile(const FusedParams& p, int t) {
   int si = 0;
   while (si + 1 < p.n_seg && t >= p.seg[si + 1].first) ++si;
   const FusedSeg& s = p.seg[si];
-  const int l = t - s.first;
+  int l = t - s.first;
+  if (!dbg_ok(l >= 0 && l < s.num_tiles, p.err_word)) l = 0;
   int mb, nb;
   if (s.m_fastest) {
     if (s.m_band > 0 && s.m_band < s.m_blocks) {
@@ -118,6 +119,11 @@ __device__ __forceinline__ FusedTile fused_tile(const FusedParams& p, int t) {
   } else {
     nb = l % s.n_blocks;
     mb = l / s.n_blocks;
+  }
+  // debug build: a tile outside its GEMM's grid is replaced by tile (0, 0)
+  if (!dbg_ok(mb >= 0 && mb < s.m_blocks && nb >= 0 && nb < s.n_blocks, p.err_word)) {
+    mb = 0;
+    nb = 0;
   }
   return {s.kind, mb, nb, (s.k_size + BK - 1) / BK, si};
 }
@@ -168,7 +174,7 @@ __device__ __forceinline__ bool fused_mma_tile(uint32_t d_tmem, int num_kb, uint
                                                uint64_t* full, uint64_t* empty, uint32_t& it,
                                                const WaitCtx& ctx) {
   using Cfg = TileCfg<true>;
-  constexpr uint32_t idesc = make_idesc(false, A_MN, B_MN, Cfg::TILE_M, BN);
+  constexpr uint32_t idesc = make_idesc(A_MN, B_MN, Cfg::TILE_M, BN);
   for (int kb = 0; kb < num_kb; ++kb) {
     const int s = it % STAGES;
     const uint32_t r = it / STAGES;
@@ -379,7 +385,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         const int row = ft.mb * Cfg::TILE_M + row_in_tile;
         const bool row_ok = row < sg.m_size;
         const long long label = row_ok ? (long long)p.labels[row] : (long long)p.ignore_index;
-        const bool valid = row_ok && label != p.ignore_index;
+        // out-of-range labels count as ignored (see the dZ epilogue of gemm_core.cuh)
+        const bool valid =
+            row_ok && label != p.ignore_index && label >= 0 && label < (long long)p.vocab;
         const long long lab_rel = label - p.col_base;
         const DzRow dzr =
             dz_row(valid, row_ok ? p.lse[row] : 0.f, c_scale, p.smoothing, p.z_loss, p.vocab);

@@ -22,8 +22,9 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
-#include <cmath>
 #include <atomic>
+#include <cmath>
+#include <cstddef>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -50,9 +51,27 @@ constexpr size_t kAlign = 256;
 
 thread_local std::string g_last_cuda_error;
 thread_local int g_launches = 0;
+// Process-wide defaults of the launch settings; a call whose options set a
+// field itself does not read the matching default.
 std::atomic<int64_t> g_vocab_chunk{0};
 std::atomic<int> g_cta_pair{1};
 std::atomic<int> g_bwd_merge{0};
+std::atomic<int> g_l2_hints{0};
+
+// Launch settings of one call, resolved once at its entry from its options
+// and the process-wide defaults, and used for both the workspace plan and the
+// launches.
+struct Tuning {
+  bool pair;           // 256 x 256 CTA-pair tiles (else 128 x 256 single-CTA)
+  bool merge;          // merged backward launches (only with pair tiles)
+  bool l2_hints;       // evict_last policy on the re-read operand
+  int64_t chunk_set;   // requested vocabulary chunk width (0 = automatic)
+};
+
+Tuning default_tuning() {
+  return Tuning{g_cta_pair.load() != 0, g_bwd_merge.load() != 0, g_l2_hints.load() != 0,
+                g_vocab_chunk.load()};
+}
 
 // Optional per-kernel timing: CUDA events recorded on the caller's stream
 // around every GEMM launch (kinds: forward logits+LSE, dZ recompute, dW, dX,
@@ -122,8 +141,8 @@ bool shape_ok(int64_t N, int64_t H, int64_t V) {
 
 // Whether backward calls may take the merged launches (CTA-pair tiles only);
 // their workspace then holds two dZ buffers.
-bool merge_planned() { return g_bwd_merge.load() != 0 && g_cta_pair.load() != 0; }
-int dz_buffers() { return merge_planned() ? 2 : 1; }
+bool merge_planned(const Tuning& t) { return t.merge && t.pair; }
+int dz_buffers(const Tuning& t) { return merge_planned(t) ? 2 : 1; }
 
 // CTA pairs of a persistent launch on the current device (76 on a 152-SM
 // GB300, also the value when no device can be queried).
@@ -153,16 +172,18 @@ int64_t wave_aligned(int64_t c, int64_t H) {
 // Cv: the dZ buffers together take at most kDzBudget (default) and at most
 // half of the N x V logits (each buffer at most V / (2 * buffers) columns); the
 // default width is wave-aligned for the three-launch backward.
-int64_t auto_chunk(int64_t N, int64_t H, int64_t V) {
-  const int64_t half = std::max<int64_t>(256, (V / (2 * dz_buffers())) / 256 * 256);
-  int64_t set = g_vocab_chunk.load();
+int64_t auto_chunk(int64_t N, int64_t H, int64_t V, const Tuning& t) {
+  const int bufs = dz_buffers(t);
+  const int64_t half = std::max<int64_t>(256, (V / (2 * bufs)) / 256 * 256);
+  const int64_t set = t.chunk_set;
   if (set > 0) return std::min(std::max<int64_t>(ceil_div(set, 256) * 256, 256), half);
-  int64_t c = (kDzBudget / dz_buffers() / (std::max<int64_t>(N, 1) * 2)) / 256 * 256;
+  int64_t c = (kDzBudget / bufs / (std::max<int64_t>(N, 1) * 2)) / 256 * 256;
   c = std::min(std::max<int64_t>(c, 256), half);
-  return merge_planned() ? c : wave_aligned(c, H);
+  return merge_planned(t) ? c : wave_aligned(c, H);
 }
 
-bool make_plan(int64_t N, int64_t H, int64_t V, flce_dtype dtype, int mode, Plan* pl) {
+bool make_plan(int64_t N, int64_t H, int64_t V, flce_dtype dtype, int mode, const Tuning& t,
+               Plan* pl) {
   if (!shape_ok(N, H, V)) return false;
   if (dtype != FLCE_BF16 && dtype != FLCE_FP32) return false;
   if (mode < FLCE_MODE_FWD || mode > FLCE_MODE_FWD_BWD) return false;
@@ -178,9 +199,9 @@ bool make_plan(int64_t N, int64_t H, int64_t V, flce_dtype dtype, int mode, Plan
   p.group_len = L;
   p.n_groups = (int)ceil_div(p.v_tiles, L);
   p.merge_blocks = (int)ceil_div(std::max<int64_t>(N, 1), MERGE_THREADS);
-  p.chunk = auto_chunk(N, H, V);
+  p.chunk = auto_chunk(N, H, V, t);
   p.n_chunks = (int)ceil_div(V, p.chunk);
-  p.dz_bufs = dz_buffers();
+  p.dz_bufs = dz_buffers(t);
   const bool fwd = mode & FLCE_MODE_FWD;
   const bool bwd = mode & FLCE_MODE_BWD;
   size_t off = 0;
@@ -230,6 +251,47 @@ bool make_plan(int64_t N, int64_t H, int64_t V, flce_dtype dtype, int mode, Plan
   p.total = off;
   return true;
 }
+
+#ifdef FLCE_DEBUG
+// Debug build: the regions a call of `mode` uses lie inside the plan's total,
+// in ascending order, without overlap, and the dZ chunk width is at most half
+// the vocabulary (or the 256-column minimum).
+bool plan_regions_ok(const Plan& p, flce_dtype dtype, int mode) {
+  struct R {
+    size_t off, bytes;
+  };
+  const size_t n1 = (size_t)std::max<int64_t>(p.N, 1);
+  std::vector<R> rs;
+  rs.push_back({p.off_scalars, kAlign});
+  rs.push_back({p.off_blocks, (size_t)(2 * p.n_blocks128 + 1) * sizeof(int)});
+  if (mode & FLCE_MODE_FWD) {
+    rs.push_back({p.off_partials, (size_t)p.n_groups * p.m_pad * sizeof(float4)});
+    rs.push_back({p.off_block_loss, (size_t)p.merge_blocks * sizeof(double)});
+    rs.push_back({p.off_block_valid, (size_t)p.merge_blocks * sizeof(int)});
+  }
+  if (mode & FLCE_MODE_BWD) {
+    rs.push_back({p.off_dz, n1 * (size_t)p.chunk * 2});
+    if (p.dz_bufs == 2) {
+      rs.push_back({p.off_dz2, n1 * (size_t)p.chunk * 2});
+      rs.push_back({p.off_counters, (size_t)p.n_chunks * sizeof(int)});
+    }
+    if (dtype == FLCE_BF16) rs.push_back({p.off_dxacc, (size_t)p.N * p.H * 4});
+    rs.push_back({p.off_mask_x, (size_t)ceil_div((int64_t)n1, BM) * p.mask_x_ld});
+    rs.push_back({p.off_mask_w, (size_t)ceil_div(p.chunk, BM) * p.mask_w_ld});
+  }
+  if (dtype == FLCE_FP32) {
+    rs.push_back({p.off_xcast, (size_t)p.N * p.H * 2});
+    rs.push_back({p.off_wcast, (size_t)p.V * p.H * 2});
+  }
+  size_t end = 0;
+  for (const R& r : rs) {
+    if (r.off < end || r.off % kAlign != 0 || r.off + r.bytes > p.total) return false;
+    end = r.off + r.bytes;
+  }
+  return p.chunk >= 256 && p.chunk % 256 == 0 && p.chunk <= std::max<int64_t>(256, p.V / 2) &&
+         p.n_chunks * p.chunk >= p.V && (int64_t)p.m_pad >= p.N;
+}
+#endif
 
 // ---------------------------------------------------------------------------
 // Device properties and kernel attributes (cached per device).
@@ -323,6 +385,34 @@ flce_status map_f32_out(CUtensorMap* m, const void* base, uint64_t cols, uint64_
                   32);
 }
 
+// One-time set-up of a kernel on one device: its dynamic shared-memory limit
+// and, for cluster kernels, how many 2-CTA clusters of it fit at once.  Done
+// under call_once, and the outcome -- a CUDA error included -- is kept, so
+// every later call on that device sees the same result.
+struct KernelSetup {
+  std::once_flag once;
+  cudaError_t err = cudaSuccess;
+  const char* what = "";
+  int max_clusters = 0;
+};
+
+template <typename Kern>
+void setup_kernel(KernelSetup& ks, Kern kern, int smem, bool cluster, int num_sms) {
+  std::call_once(ks.once, [&] {
+    ks.err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    ks.what = "cudaFuncSetAttribute";
+    if (ks.err != cudaSuccess || !cluster) return;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    int n = 0;
+    ks.err = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    ks.what = "cudaOccupancyMaxActiveClusters";
+    ks.max_clusters = std::max(1, std::min(n, num_sms / 2));
+  });
+}
+
 template <Epi EPI, bool A_MN, bool B_MN, bool PAIR, bool EXT>
 flce_status launch_gemm(int dev, int num_sms, const CUtensorMap& a, const CUtensorMap& b,
                         const CUtensorMap& out, const GemmParams& p, cudaStream_t st,
@@ -335,30 +425,15 @@ flce_status launch_gemm(int dev, int num_sms, const CUtensorMap& a, const CUtens
       return gemm_kernel<EPI, A_MN, B_MN, stages, EXT>;
   }();
   constexpr int smem = gemm_smem_bytes<EPI, stages, PAIR, EXT>();
-  static std::once_flag flags[kMaxDevices];
-  cudaError_t attr_err = cudaSuccess;
-  std::call_once(flags[dev], [&] {
-    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  });
-  if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute");
+  static KernelSetup setup[kMaxDevices];
+  setup_kernel(setup[dev], kern, smem, PAIR, num_sms);
+  if (setup[dev].err != cudaSuccess) return cuda_fail(setup[dev].err, setup[dev].what);
   if (p.num_units <= 0) return FLCE_OK;
   // One CTA per SM (one cluster per SM pair), persistent over the work units.
   // A persistent grid must be co-resident, so pairs are capped by how many
   // 2-CTA clusters of this size fit on the device at once.
   int grid = std::min(p.num_units, num_sms);
-  if constexpr (PAIR) {
-    static int max_clusters[kMaxDevices] = {0};
-    if (max_clusters[dev] == 0) {
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
-      cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-      cfg.dynamicSmemBytes = smem;
-      int n = 0;
-      FLCE_CUDA(cudaOccupancyMaxActiveClusters(&n, kern, &cfg));
-      max_clusters[dev] = std::max(1, std::min(n, num_sms / 2));
-    }
-    grid = 2 * std::min(p.num_units, max_clusters[dev]);
-  }
+  if constexpr (PAIR) grid = 2 * std::min(p.num_units, setup[dev].max_clusters);
   ProfRec rec{prof_kind, nullptr, nullptr};
   if (g_prof_on && prof_kind >= 0) {
     rec.start = prof_event();
@@ -387,32 +462,17 @@ flce_status launch_tile(bool pair, bool ext, int dev, int num_sms, const CUtenso
               : launch_gemm<EPI, A_MN, B_MN, false, false>(dev, num_sms, a, b, out, p, st, prof_kind);
 }
 
-bool use_pair() { return g_cta_pair.load() != 0; }
-
 // One merged backward launch (CTA pairs, persistent; the list's tiles go round
 // robin except the last DYNAMIC_ROUNDS rounds, taken from a global counter).
 flce_status launch_fused(int dev, int num_sms, const FusedMaps& maps, const FusedParams& p,
                          cudaStream_t st) {
   constexpr int smem = fused_smem_bytes<kPairStages>();
   auto kern = bwd_fused_kernel<kPairStages>;
-  static std::once_flag flags[kMaxDevices];
-  cudaError_t attr_err = cudaSuccess;
-  std::call_once(flags[dev], [&] {
-    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  });
-  if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute");
+  static KernelSetup setup[kMaxDevices];
+  setup_kernel(setup[dev], kern, smem, true, num_sms);
+  if (setup[dev].err != cudaSuccess) return cuda_fail(setup[dev].err, setup[dev].what);
   if (p.total_tiles <= 0) return FLCE_OK;
-  static int max_clusters[kMaxDevices] = {0};
-  if (max_clusters[dev] == 0) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
-    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    int n = 0;
-    FLCE_CUDA(cudaOccupancyMaxActiveClusters(&n, kern, &cfg));
-    max_clusters[dev] = std::max(1, std::min(n, num_sms / 2));
-  }
-  const int pairs = std::min(p.total_tiles, max_clusters[dev]);
+  const int pairs = std::min(p.total_tiles, setup[dev].max_clusters);
   const int grid = 2 * pairs;
   // all but the last DYNAMIC_ROUNDS rounds of tiles go round robin
   FusedParams pp = p;
@@ -449,9 +509,8 @@ int x_band(int64_t N, int64_t H, int m_blocks) {
 
 // Fraction of the reused operand's lines kept in L2 with evict_last priority:
 // about 64 MB of the 129 MB L2 is given to it, the rest streams.
-std::atomic<int> g_l2_hints{0};
-float l2_keep_fraction(double operand_bytes) {
-  if (!g_l2_hints.load() || operand_bytes <= 0) return 0.f;
+float l2_keep_fraction(const Tuning& t, double operand_bytes) {
+  if (!t.l2_hints || operand_bytes <= 0) return 0.f;
   return (float)std::min(1.0, (64.0 * (1 << 20)) / operand_bytes);
 }
 int tile_rows(bool pair) { return pair ? 2 * BM : BM; }
@@ -486,6 +545,7 @@ struct Common {
   int64_t vocab_offset = 0;
   int64_t vocab_total = 0;
   bool dx_partial_f32 = false;
+  Tuning tun{};
 };
 
 flce_status validate_common(const Common& c, int mode, Plan* pl) {
@@ -503,15 +563,21 @@ flce_status validate_common(const Common& c, int mode, Plan* pl) {
   }
   if (!c.W || !aligned(c.W, 16)) return FLCE_ERR_ARG;
   if (!aligned(c.err_word, 4)) return FLCE_ERR_ARG;
-  if (!make_plan(c.N, c.H, c.V, c.dtype, mode, pl)) return FLCE_ERR_ARG;
+  if (!make_plan(c.N, c.H, c.V, c.dtype, mode, c.tun, pl)) return FLCE_ERR_ARG;
   if (!c.ws || !aligned(c.ws, kAlign)) return FLCE_ERR_WORKSPACE;
   if (c.ws_bytes < pl->total) return FLCE_ERR_WORKSPACE;
+#ifdef FLCE_DEBUG
+  if (!plan_regions_ok(*pl, c.dtype, mode)) {
+    g_last_cuda_error = "debug build: workspace plan regions overlap or overrun";
+    return FLCE_ERR_BOUNDS;
+  }
+#endif
   return FLCE_OK;
 }
 
 // Whether a call needs the kernels' optional features compiled in.
 bool ext_features(const Common& c) {
-  return c.skip_ignored || c.grad_filter > 0.f || g_l2_hints.load() != 0;
+  return c.skip_ignored || c.grad_filter > 0.f || c.tun.l2_hints;
 }
 
 // Skip lists for SFT-style masking: token blocks of `tile_rows(pair)` rows with
@@ -574,7 +640,7 @@ flce_status run_forward(const Common& c, const Plan& pl, int dev, int sms, const
   double* block_loss = reinterpret_cast<double*>(ws + pl.off_block_loss);
   int* block_valid = reinterpret_cast<int*>(ws + pl.off_block_valid);
   if (c.N > 0) {
-    const bool pair = use_pair();
+    const bool pair = c.tun.pair;
     SkipLists sk;
     FLCE_TRY(build_skip_lists(c, pl, pair, &sk));
     CUtensorMap tmX, tmW;
@@ -600,9 +666,10 @@ flce_status run_forward(const Common& c, const Plan& pl, int dev, int sms, const
     p.partials = reinterpret_cast<float4*>(ws + pl.off_partials);
     p.m_pad = pl.m_pad;
     p.l2_keep_b = 0;
-    p.l2_keep_frac = l2_keep_fraction((double)c.N * c.H * 2);
+    p.l2_keep_frac = l2_keep_fraction(c.tun, (double)c.N * c.H * 2);
     p.row_list = sk.list;
     p.row_count = sk.count;
+    p.list_cap = pl.n_blocks128;
     p.err_word = c.err_word;
     p.timeout_ns = kTimeoutNs;
     FLCE_TRY((launch_tile<Epi::kLse, false, false>(pair, ext_features(c), dev, sms, tmX, tmW, tmX, p,
@@ -654,7 +721,7 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
   FLCE_TRY(map_mnmajor(&tmX_mn, Xb, H, N, H));
   FLCE_TRY(map_f32_out(&tmDxAcc, dx_acc, H, N, H));
 
-  const bool pair = use_pair();
+  const bool pair = c.tun.pair;
   const bool ext = ext_features(c);
   const int m_blocks_tok = (int)ceil_div(N, tile_rows(pair));
   SkipLists sk;
@@ -696,6 +763,7 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
     p3.z_loss = c.z_loss;
     p3.row_list = sk.list;
     p3.row_count = sk.count;
+    p3.list_cap = pl.n_blocks128;
     if (filt) {
       p3.mask_x_out = mask_x;
       p3.mask_w_out = mask_w;
@@ -703,11 +771,13 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
       p3.mask_w_ld = pl.mask_w_ld;
       p3.mask_tile = tile_rows(pair);
       p3.filter_thr = c.grad_filter;
+      p3.mask_x_bytes = (long long)mask_x_bytes;
+      p3.mask_w_bytes = (long long)mask_w_bytes;
     }
     p3.lse = lse;
     p3.scale = scale;
     p3.l2_keep_b = 0;  // X is reused by every wave; the W tile is shared within one
-    p3.l2_keep_frac = l2_keep_fraction((double)N * H * 2);
+    p3.l2_keep_frac = l2_keep_fraction(c.tun, (double)N * H * 2);
     p3.err_word = c.err_word;
     p3.timeout_ns = kTimeoutNs;
     return p3;
@@ -834,12 +904,14 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
       p4.k_list = sk.list;
       p4.k_count = sk.count;
       p4.k_per_entry = tile_rows(pair) / BK;
+      p4.list_cap = pl.n_blocks128;
       if (filt) {
         p4.fmask = mask_w;
         p4.fmask_ld = pl.mask_w_ld;
+        p4.fmask_bytes = (long long)mask_w_bytes;
       }
       p4.l2_keep_b = 1;  // X again; the dZ column block is shared within one wave
-      p4.l2_keep_frac = l2_keep_fraction((double)N * H * 2);
+      p4.l2_keep_frac = l2_keep_fraction(c.tun, (double)N * H * 2);
       p4.err_word = c.err_word;
       p4.timeout_ns = kTimeoutNs;
       FLCE_TRY((launch_tile<Epi::kStore, true, true>(pair, ext, dev, sms, tmDz_mn, tmX_mn, tmDw, p4,
@@ -859,12 +931,14 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
       p5.reduce_add = ci > 0 ? 1 : 0;
       p5.row_list = sk.list;
       p5.row_count = sk.count;
+      p5.list_cap = pl.n_blocks128;
       if (filt) {
         p5.fmask = mask_x;
         p5.fmask_ld = pl.mask_x_ld;
+        p5.fmask_bytes = (long long)mask_x_bytes;
       }
       p5.l2_keep_b = 1;  // the W chunk; the dZ row block is shared within one wave
-      p5.l2_keep_frac = l2_keep_fraction((double)w * H * 2);
+      p5.l2_keep_frac = l2_keep_fraction(c.tun, (double)w * H * 2);
       p5.err_word = c.err_word;
       p5.timeout_ns = kTimeoutNs;
       FLCE_TRY((launch_tile<Epi::kStore, false, true>(pair, ext, dev, sms, tmDz_k, tmWc_mn, tmDxAcc,
@@ -889,7 +963,7 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
 // ===========================================================================
 extern "C" {
 
-int flce_abi_version(void) { return 105; }
+int flce_abi_version(void) { return 106; }
 
 const char* flce_status_string(flce_status s) {
   switch (s) {
@@ -900,6 +974,7 @@ const char* flce_status_string(flce_status s) {
     case FLCE_ERR_LABEL: return "FLCE_ERR_LABEL: label outside [0, V) and not ignore_index";
     case FLCE_ERR_TIMEOUT: return "FLCE_ERR_TIMEOUT: a bounded device wait expired";
     case FLCE_ERR_CUDA: return "FLCE_ERR_CUDA: CUDA call failed";
+    case FLCE_ERR_BOUNDS: return "FLCE_ERR_BOUNDS: an index check of the debug build failed";
   }
   return "unknown flce_status";
 }
@@ -969,12 +1044,12 @@ flce_status flce_set_vocab_chunk(int64_t cols) {
 
 int64_t flce_vocab_chunk(int64_t N, int64_t H, int64_t V) {
   if (N < 0 || H <= 0 || V <= 0) return 0;
-  return auto_chunk(N, H, V);
+  return auto_chunk(N, H, V, default_tuning());
 }
 
 size_t flce_workspace_size(int64_t N, int64_t H, int64_t V, flce_dtype dtype, int mode) {
   Plan pl;
-  if (!make_plan(N, H, V, dtype, mode, &pl)) return 0;
+  if (!make_plan(N, H, V, dtype, mode, default_tuning(), &pl)) return 0;
   return pl.total;
 }
 
@@ -988,14 +1063,38 @@ void flce_options_init(flce_options* opt) {
   opt->row_loss = nullptr;
   opt->skip_ignored_blocks = 0;
   opt->grad_filter = 0.f;
+  opt->cta_pair = -1;
+  opt->backward_merge = -1;
+  opt->l2_hints = -1;
+  opt->vocab_chunk = -1;
 }
 
 }  // extern "C"
 
 namespace {
 
+// Size of the options struct of ABI 1.05, before the launch settings.
+constexpr size_t kOptionsV105Size = offsetof(flce_options, cta_pair);
+
 bool options_ok(const flce_options* opt) {
-  return opt && opt->struct_size == sizeof(flce_options);
+  if (!opt) return false;
+  if (opt->struct_size == kOptionsV105Size) return true;
+  if (opt->struct_size != sizeof(flce_options)) return false;
+  auto tri = [](int v) { return v >= -1 && v <= 1; };
+  return tri(opt->cta_pair) && tri(opt->backward_merge) && tri(opt->l2_hints) &&
+         opt->vocab_chunk >= -1;
+}
+
+// The launch settings of a call: each options field that is not -1 overrides
+// the process-wide default (a 1.05-sized struct has no such fields).
+Tuning resolve_tuning(const flce_options* opt) {
+  Tuning t = default_tuning();
+  if (!opt || opt->struct_size < sizeof(flce_options)) return t;
+  if (opt->cta_pair >= 0) t.pair = opt->cta_pair != 0;
+  if (opt->backward_merge >= 0) t.merge = opt->backward_merge != 0;
+  if (opt->l2_hints >= 0) t.l2_hints = opt->l2_hints != 0;
+  if (opt->vocab_chunk >= 0) t.chunk_set = opt->vocab_chunk;
+  return t;
 }
 
 Common make_common(const void* X, const void* W, const int64_t* labels, int64_t N, int64_t H,
@@ -1021,7 +1120,8 @@ Common make_common(const void* X, const void* W, const int64_t* labels, int64_t 
                 static_cast<cudaStream_t>(stream),
                 0,
                 V,
-                false};
+                false,
+                resolve_tuning(o)};
 }
 
 flce_options defaults(int64_t ignore_index, float smoothing, flce_reduction reduction) {
@@ -1036,6 +1136,20 @@ flce_options defaults(int64_t ignore_index, float smoothing, flce_reduction redu
 }  // namespace
 
 extern "C" {
+
+size_t flce_workspace_size_ex(int64_t N, int64_t H, int64_t V, flce_dtype dtype, int mode,
+                              const flce_options* opt) {
+  if (opt && !options_ok(opt)) return 0;
+  Plan pl;
+  if (!make_plan(N, H, V, dtype, mode, resolve_tuning(opt), &pl)) return 0;
+  return pl.total;
+}
+
+int64_t flce_vocab_chunk_ex(int64_t N, int64_t H, int64_t V, const flce_options* opt) {
+  if (N < 0 || H <= 0 || V <= 0) return 0;
+  if (opt && !options_ok(opt)) return 0;
+  return auto_chunk(N, H, V, resolve_tuning(opt));
+}
 
 flce_status flce_forward_ex(const void* X, const void* W, const int64_t* labels, int64_t N,
                             int64_t H, int64_t V, flce_dtype dtype, const flce_options* opt,
@@ -1279,14 +1393,14 @@ flce_status flce_debug_gemm(const void* A, const void* B, float* D, int64_t M, i
   CUtensorMap ta, tb, td;
   if (a_mn) FLCE_TRY(map_mnmajor(&ta, A, M, K, M));
   else FLCE_TRY(map_kmajor(&ta, A, K, M, K, BM));
+  const bool pair = g_cta_pair.load() != 0;
   if (b_mn) FLCE_TRY(map_mnmajor(&tb, B, Nn, K, Nn));
-  else FLCE_TRY(map_kmajor(&tb, B, K, Nn, K, b_box_rows(use_pair())));
+  else FLCE_TRY(map_kmajor(&tb, B, K, Nn, K, b_box_rows(pair)));
   FLCE_TRY(map_f32_out(&td, D, Nn, M, Nn));
   GemmParams p{};
   p.m_size = (int)M;
   p.n_size = (int)Nn;
   p.k_size = (int)K;
-  const bool pair = use_pair();
   p.m_blocks = (int)ceil_div(M, tile_rows(pair));
   p.n_blocks = (int)ceil_div(Nn, BN);
   p.group_len = 1;

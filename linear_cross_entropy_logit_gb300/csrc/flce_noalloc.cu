@@ -19,10 +19,13 @@
 // caches it; make that first call before any stream capture.
 //
 // All calls share the one array and it keeps the last call's contents.
-// Nothing in it has to start at zero: every slot a call reads was written
-// earlier in that same call.  Two calls whose kernels overlap on the GPU
-// (different streams, or different host threads) race on the array and give
-// wrong results; serialise them.
+// Nothing in it has to start at zero: in a call that completes normally,
+// every slot the merge reads was written earlier in that same call.  After a
+// bounded wait expired (FLCE_ERR_TIMEOUT in the error word) the GEMM skips
+// its partial writes, so the merge may read an earlier call's partials: loss
+// and lse are then undefined, as the header states.  Two calls whose kernels
+// overlap on the GPU (different streams, or different host threads) race on
+// the array and give wrong results; serialise them.
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
@@ -173,7 +176,11 @@ extern "C" flce_status flce_forward_noalloc(const void* X, const void* W, const 
   if (reduction != FLCE_MEAN && reduction != FLCE_SUM) return FLCE_ERR_ARG;
   if (!(smoothing >= 0.f && smoothing < 1.f)) return FLCE_ERR_ARG;
   if (!W || !na_aligned(W, 16) || !loss || !valid_count || !err_word) return FLCE_ERR_ARG;
-  if (N > 0 && (!X || !labels || !lse || !na_aligned(X, 16) || !na_aligned(labels, 8)))
+  // the merge and loss kernels store these as 32-bit words
+  if (!na_aligned(err_word, 4) || !na_aligned(loss, 4) || !na_aligned(valid_count, 4))
+    return FLCE_ERR_ARG;
+  if (N > 0 && (!X || !labels || !lse || !na_aligned(X, 16) || !na_aligned(labels, 8) ||
+                !na_aligned(lse, 4)))
     return FLCE_ERR_ARG;
   NaPlan pl;
   if (!na_plan(N, V, &pl)) {

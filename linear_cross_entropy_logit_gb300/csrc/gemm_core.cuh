@@ -110,6 +110,7 @@ struct GemmParams {
   const int* k_list;
   const int* k_count;
   int k_per_entry;
+  int list_cap;       // entries row_list / k_list hold (index checks of the debug build)
   // Gradient filtering (CCE-style).  The kDz launch marks, for every
   // 32-token x 64-column block of dZ that holds a probability >= filter_thr
   // or a target, maskX[token tile][vocab k-block] and maskW[vocab tile][token
@@ -122,8 +123,11 @@ struct GemmParams {
   int mask_w_ld;      // token k-blocks per vocabulary tile
   int mask_tile;      // rows of the dX / dW tiles the masks describe
   float filter_thr;
+  long long mask_x_bytes;  // sizes of the two masks (index checks of the debug build)
+  long long mask_w_bytes;
   const uint8_t* fmask;
   int fmask_ld;
+  long long fmask_bytes;   // size of fmask (index checks of the debug build)
   // L2 residency: the operand reused across waves of tiles (0 = A, 1 = B) is
   // loaded with an evict_last policy covering `l2_keep_frac` of its lines.
   int l2_keep_b;
@@ -150,7 +154,8 @@ struct UnitSpace {
 
 __device__ __forceinline__ UnitSpace unit_space(const GemmParams& p) {
   if (p.row_list) {
-    const int cnt = *p.row_count;
+    int cnt = *p.row_count;
+    if (!dbg_ok(cnt >= 0 && cnt <= p.list_cap, p.err_word)) cnt = 0;
     return {cnt, cnt * p.n_groups};
   }
   return {p.m_blocks, p.num_units};
@@ -178,19 +183,35 @@ __device__ __forceinline__ void unit_coords(const GemmParams& p, const UnitSpace
     mb = u / p.n_groups;
   }
   if constexpr (EXT) {
-    if (p.row_list) mb = p.row_list[mb];
+    if (p.row_list) mb = dbg_ok(mb >= 0 && mb < us.m_blocks, p.err_word) ? p.row_list[mb] : 0;
   }
   nb0 = g * p.group_len;
   nb1 = min(nb0 + p.group_len, p.n_blocks);
+  // debug build: a unit outside the tile grid gets no tiles (every role of
+  // the CTA computes the same coordinates, so all of them skip it)
+  if (!dbg_ok(mb >= 0 && mb < p.m_blocks && g >= 0 && g < p.n_groups && nb0 < p.n_blocks,
+              p.err_word)) {
+    mb = 0;
+    g = 0;
+    nb0 = nb1 = 0;
+  }
 }
 
 // Number of k-blocks the contraction walks, and the i-th of them.
 __device__ __forceinline__ int kblock_count(const GemmParams& p, int num_kb) {
-  return p.k_list ? (*p.k_count) * p.k_per_entry : num_kb;
+  if (!p.k_list) return num_kb;
+  int cnt = *p.k_count;
+  if (!dbg_ok(cnt >= 0 && cnt <= p.list_cap, p.err_word)) cnt = 0;
+  return cnt * p.k_per_entry;
 }
 
+// (debug build: a k-block outside [0, ceil(k_size / BK)) is replaced by 0)
 __device__ __forceinline__ int kblock_at(const GemmParams& p, int i) {
-  return p.k_list ? p.k_list[i / p.k_per_entry] * p.k_per_entry + i % p.k_per_entry : i;
+  if (!p.k_list) return i;
+  const int e = i / p.k_per_entry;
+  if (!dbg_ok(e >= 0 && e < p.list_cap, p.err_word)) return 0;
+  const int kb = p.k_list[e] * p.k_per_entry + i % p.k_per_entry;
+  return dbg_ok(kb >= 0 && kb < (p.k_size + BK - 1) / BK, p.err_word) ? kb : 0;
 }
 
 // Gradient filtering: copy the keep bytes of row block mb's tile into shared
@@ -202,11 +223,23 @@ __device__ __forceinline__ int load_tile_keep(const GemmParams& p, int mb, int n
   if (!p.k_list) {
     const uint4* src = reinterpret_cast<const uint4*>(row);
     const int n16 = (num_kb + 15) / 16;
+    if (dbg_ok((long long)mb * p.fmask_ld + n16 * 16 <= p.fmask_bytes && n16 * 16 <= FILTER_MAX_KB,
+               p.err_word)) {
 #pragma unroll 4
-    for (int i = 0; i < n16; ++i) reinterpret_cast<uint4*>(keep)[i] = __ldg(src + i);
+      for (int i = 0; i < n16; ++i) reinterpret_cast<uint4*>(keep)[i] = __ldg(src + i);
+    } else {
+      for (int i = 0; i < num_kb && i < FILTER_MAX_KB; ++i) keep[i] = 1;
+    }
   } else {
 #pragma unroll 4
-    for (int i = 0; i < num_kb; ++i) keep[i] = __ldg(row + kblock_at(p, i));
+    for (int i = 0; i < num_kb; ++i) {
+      const int kb = kblock_at(p, i);
+      keep[i] = dbg_ok(i < FILTER_MAX_KB && kb < p.fmask_ld &&
+                           (long long)mb * p.fmask_ld + kb < p.fmask_bytes,
+                       p.err_word)
+                    ? __ldg(row + kb)
+                    : (uint8_t)1;
+    }
   }
   keep[0] = 1;
   int last = num_kb - 1;
@@ -530,7 +563,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && rank == 0) {
-      constexpr uint32_t idesc = make_idesc(false, A_MN, B_MN, Cfg::TILE_M, BN);
+      constexpr uint32_t idesc = make_idesc(A_MN, B_MN, Cfg::TILE_M, BN);
       // MN-major operand blocks are 64 elements wide; LBO = distance between them.
       constexpr uint32_t kMnLbo = MN_BOX_BYTES;
       uint32_t it = 0, tile = 0;
@@ -569,7 +602,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
               if constexpr (PAIR)
                 mma_issue_pair(d_tmem, ad, bd, idesc, (ki | kk) != 0 ? 1u : 0u);
               else
-                mma_issue<false>(d_tmem, ad, bd, idesc, (ki | kk) != 0 ? 1u : 0u);
+                mma_issue(d_tmem, ad, bd, idesc, (ki | kk) != 0 ? 1u : 0u);
             }
             if constexpr (PAIR)
               mma_commit_pair_multicast(&empty[s], 0x3);
@@ -617,7 +650,10 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
       long long label = 0;
       if constexpr (EPI != Epi::kStore)
         label = row_ok ? (long long)p.labels[row] : (long long)p.ignore_index;
-      const bool valid = row_ok && label != p.ignore_index;
+      // A label outside [0, V) that is not ignore_index counts as ignored, as
+      // in the forward's merge (which records FLCE_ERR_LABEL for it).
+      const bool valid =
+          row_ok && label != p.ignore_index && label >= 0 && label < (long long)p.vocab;
       const long long lab_rel = label - p.col_base;
 
       DzRow dzr{};
@@ -684,8 +720,12 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
               // probability >= the threshold or its target in it
               const bool keep_row = valid && (pmax >= p.filter_thr || (off >= 0 && off < 64));
               if (__ballot_sync(0xffffffffu, keep_row) != 0u && lane == 0) {
-                p.mask_x_out[(size_t)(store_row0 / p.mask_tile) * p.mask_x_ld + c0 / 64] = 1;
-                p.mask_w_out[(size_t)(c0 / p.mask_tile) * p.mask_w_ld + store_row0 / 64] = 1;
+                const long long ix = (long long)(store_row0 / p.mask_tile) * p.mask_x_ld + c0 / 64;
+                const long long iw = (long long)(c0 / p.mask_tile) * p.mask_w_ld + store_row0 / 64;
+                if (dbg_ok(c0 / 64 < p.mask_x_ld && ix < p.mask_x_bytes, p.err_word))
+                  p.mask_x_out[ix] = 1;
+                if (dbg_ok(store_row0 / 64 < p.mask_w_ld && iw < p.mask_w_bytes, p.err_word))
+                  p.mask_w_out[iw] = 1;
               }
             }
             staged_store(stag0 + (nstore++ & 1u) * STAGING_BUF_BYTES, staging, lane, w, &tmOut,
@@ -721,7 +761,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
       }
 
       if constexpr (EPI == Epi::kLse) {
-        if (ok) p.partials[(size_t)g * p.m_pad + row] = make_float4(m2, ssum, zy, zsum);
+        if (ok && dbg_ok(g < p.n_groups && row < p.m_pad, p.err_word))
+          p.partials[(size_t)g * p.m_pad + row] = make_float4(m2, ssum, zy, zsum);
       }
     }
     if constexpr (EPI != Epi::kLse) {

@@ -12,7 +12,7 @@
 namespace flce {
 
 // Error codes shared with include/flce.h (kept numerically identical).
-enum : int { kErrLabel = 4, kErrTimeout = 5 };
+enum : int { kErrLabel = 4, kErrTimeout = 5, kErrBounds = 7 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -26,6 +26,23 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 
 __device__ __forceinline__ void record_error(int* err_word, int code) {
   if (err_word) atomicCAS(err_word, 0, code);
+}
+
+// Index check of the debug build (FLCE_DEBUG): returns whether an index about
+// to be used is in range; if it is not, FLCE_ERR_BOUNDS is recorded and the
+// caller skips or clamps the access.  Without FLCE_DEBUG it is always true
+// and the check compiles away.
+__device__ __forceinline__ bool dbg_ok(bool in_range, int* err_word) {
+#ifdef FLCE_DEBUG
+  if (!in_range) {
+    record_error(err_word, kErrBounds);
+    return false;
+  }
+#else
+  (void)in_range;
+  (void)err_word;
+#endif
+  return true;
 }
 
 // ----------------------------------------------------------------------------
@@ -233,23 +250,14 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, one instruction of kind::f16 or kind::tf32.
-template <bool kTf32>
+// D[tmem] (+)= A[smem] * B[smem]^T, one instruction of kind::f16 (bf16 A and B).
 __device__ __forceinline__ void mma_issue(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                           uint32_t idesc, uint32_t accumulate) {
-  if constexpr (kTf32) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}"
-        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-  } else {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-  }
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
 }
 
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far
@@ -302,16 +310,12 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
-// Instruction descriptor for kind::f16 (bf16 inputs) or kind::tf32, fp32
-// accumulate, dense.
-//   bits 4-5 D format (1 = f32); 7-9 A format; 10-12 B format
-//   (bf16 = 1 under kind::f16, tf32 = 2 under kind::tf32);
+// Instruction descriptor for kind::f16 with bf16 A and B, fp32 accumulate, dense.
+//   bits 4-5 D format (1 = f32); 7-9 A format, 10-12 B format (1 = bf16);
 //   bit 15 A MN-major; bit 16 B MN-major; bits 17-22 N >> 3; bits 24-28 M >> 4.
-__host__ __device__ constexpr uint32_t make_idesc(bool tf32, bool a_mn, bool b_mn, uint32_t M,
-                                                  uint32_t N) {
-  return (1u << 4) | ((tf32 ? 2u : 1u) << 7) | ((tf32 ? 2u : 1u) << 10) |
-         (static_cast<uint32_t>(a_mn) << 15) | (static_cast<uint32_t>(b_mn) << 16) |
-         ((N >> 3) << 17) | ((M >> 4) << 24);
+__host__ __device__ constexpr uint32_t make_idesc(bool a_mn, bool b_mn, uint32_t M, uint32_t N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn) << 15) |
+         (static_cast<uint32_t>(b_mn) << 16) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
 // ----------------------------------------------------------------------------

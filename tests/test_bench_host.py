@@ -92,7 +92,7 @@ def test_traffic_summary_and_source_gate(bench, tmp_path, monkeypatch):
     got = bench.load_traffic("wl")
     assert got["fwd_logits_lse"] == pytest.approx(100e6 + 500e3)
     assert got["bwd_dz_recompute"] == pytest.approx(200e6 + 500e3)
-    assert got["bwd_dw_gemm"] == pytest.approx((300e6 + 500e6) / 2 + 500e3)   # mean of two launches
+    assert got["bwd_dw_gemm"] == pytest.approx(500e6 + 500e3)   # the last of two launches
     assert got["bwd_dx_gemm"] == pytest.approx(400e6 + 500e3)
     assert got["bwd_merged"] == pytest.approx(600e6 + 500e3)
     assert "lse_merge" not in " ".join(got)
@@ -102,6 +102,13 @@ def test_traffic_summary_and_source_gate(bench, tmp_path, monkeypatch):
              for l in lines]
     out.write_text("\n".join(lines) + "\n")
     assert bench.load_traffic("wl") is None
+    # a capture at reduced V (same N and H) scales the forward by V_full / V
+    bench.summarize_traffic(str(csv_path), "llama3_n8192", shape=(8192, 4096, 32064))
+    got = bench.load_traffic("llama3_n8192")
+    assert got["fwd_logits_lse"] == pytest.approx((100e6 + 500e3) * 128256 / 32064)
+    assert got["bwd_dx_gemm"] == pytest.approx(400e6 + 500e3)
+    with pytest.raises(ValueError):
+        bench.summarize_traffic(str(csv_path), "llama3_n8192", shape=(4096, 4096, 32064))
 
 
 def test_peaks_measured_and_fallback(bench, tmp_path, monkeypatch):

@@ -3,10 +3,15 @@
 One flce_fwd_bwd call per workload (default vocabulary chunk).  Against the
 fp64 oracle:
   * the loss and the lse of every token row (the oracle's full forward);
-  * dX on sampled token rows, ignored rows included (exactly zero there);
-  * dW on sampled vocabulary rows (the most frequent labels, random rows, and
-    for the Gemma-shaped workload some of the x8-scaled rows), each computed
-    by the oracle one by one from its own lse;
+  * dX on sampled token rows, ignored rows included (exactly zero there): the
+    first and last row of every row-block band the forward and dZ launches
+    walk (and an ignored row inside each band), the last row N-1, and random
+    rows;
+  * dW on sampled vocabulary rows: the first and last row of every vocabulary
+    chunk of the backward (the partial last chunk included), the most
+    frequent labels, random rows, and for the Gemma-shaped workload the
+    x8-scaled rows nearest a chunk edge and some others, each computed by the
+    oracle one by one from its own lse;
   * the property sum_j dW_j = 0 (with z-loss: sum_i 2 c alpha lse_i x_i) on
     the whole GPU dW, relative to sum_j |dW_j|.
 Each case takes from ~20 s (Llama shape) to ~2 min (Gemma shape) of oracle time
@@ -23,6 +28,32 @@ pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
 WORKLOADS = [("llama3_n8192", 0.0), ("llama3_long_n16384", 0.0), ("qwen25_n16384", 0.0),
              ("gemma2_n32768", 0.0), ("llama3_n8192", 1e-4)]
+
+
+def band_edge_rows(N, H, labels, ii):
+    """Token rows at the edges of the row-block bands the forward and dZ
+    launches walk (X above 48 MiB is split into ceil(X / 40 MiB) bands of
+    256-row blocks, at most 4), plus one ignored row inside each band."""
+    blocks = -(-N // 256)
+    x_bytes = N * H * 2
+    bands = min(4, -(-x_bytes // (40 << 20))) if x_bytes > (48 << 20) else 1
+    per = -(-blocks // bands) * 256
+    rows = []
+    for b0 in range(0, N, per):
+        b1 = min(N, b0 + per)
+        rows += [b0, b1 - 1]
+        ign = np.flatnonzero(labels[b0:b1] == ii)
+        if ign.size:
+            rows.append(b0 + int(ign[len(ign) // 2]))
+    return rows + [N - 1]
+
+
+def chunk_edge_rows(V, cv):
+    """First and last vocabulary row of every backward chunk of width cv."""
+    rows = []
+    for v0 in range(0, V, cv):
+        rows += [v0, min(V, v0 + cv) - 1]
+    return rows
 
 
 @pytest.mark.parametrize("name,z_loss", WORKLOADS,
@@ -45,13 +76,18 @@ def test_full_size_parity(name, z_loss):
 
     rng = np.random.default_rng(1234)
     ignored = np.flatnonzero(wl.labels == ii)
-    rows = np.unique(np.concatenate([ignored[:8], rng.choice(N, 56, replace=False)]))
+    rows = np.unique(np.concatenate([ignored[:8], rng.choice(N, 56, replace=False),
+                                     band_edge_rows(N, spec.H, wl.labels, ii)]))
     labels_valid = wl.labels[wl.labels != ii]
     counts = np.bincount(labels_valid, minlength=V)
-    vrows = [np.argsort(-counts)[:8], rng.choice(V, 40, replace=False)]
+    cv = B.flce_vocab_chunk(N, spec.H, V)
+    edges = np.array(chunk_edge_rows(V, cv))
+    vrows = [np.argsort(-counts)[:8], rng.choice(V, 40, replace=False), edges]
     if spec.n_scaled_w_rows:
         scaled = I._rng(0, 5).permutation(V)[:spec.n_scaled_w_rows]
-        vrows.append(scaled[:8])
+        # the scaled rows nearest a chunk edge, and a few others
+        dist = np.min(np.abs(scaled[:, None] - edges[None, :]), axis=1)
+        vrows += [scaled[np.argsort(dist)[:8]], scaled[:8]]
     vrows = np.unique(np.concatenate(vrows))
     got_dx = dX[torch.from_numpy(rows).cuda()].double().cpu().numpy()
     got_dw = dW[torch.from_numpy(vrows).cuda()].double().cpu().numpy()

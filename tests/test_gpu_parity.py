@@ -180,6 +180,63 @@ def test_invalid_label_sets_error_word():
     assert int(nv.item()) == 63
 
 
+BAD_LABELS = {5: "V", 300: -1, 599: "V+7"}
+
+
+@pytest.mark.parametrize("path", ["three_launch", "merged", "vocab_shard"])
+def test_invalid_labels_count_as_ignored(path):
+    """A label outside [0, V) that is not ignore_index sets FLCE_ERR_LABEL and
+    its row counts as ignored in the forward AND the backward: loss, lse, dX
+    and dW equal the oracle's on the same labels with those entries replaced
+    by ignore_index, and the bad rows of dX are exactly zero ("Fused
+    cross-entropy -- the memory kernel", "Numerical traps": the ignore_index
+    mask folded into the fused pass)."""
+    import torch
+    from linear_cross_entropy_logit_gb300 import binding as B
+    V = 1000
+    wl = I.make_workload(spec(N=600, H=136, V=V, n_ignore=30, smoothing=0.1), seed=23)
+    bad = np.array(sorted(BAD_LABELS))
+    for r, v in BAD_LABELS.items():
+        wl.labels[r] = {"V": V, "V+7": V + 7}.get(v, v)
+    ref_labels = wl.labels.copy()
+    ref_labels[bad] = -100
+    X, W, y = to_device(wl)
+    eps = wl.spec.smoothing
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    if path == "vocab_shard":
+        opt = B.make_options(-100, eps)
+        bounds = [0, 512, V]
+        parts = torch.empty(2, wl.N, 4, dtype=torch.float32, device="cuda")
+        for i, (b0, b1) in enumerate(zip(bounds, bounds[1:])):
+            B.flce_forward_vocab_shard(X, W[b0:b1].contiguous(), y, b0, V, opt,
+                                       partials=parts[i], err_word=err)
+        loss, lse, nv, _ = B.flce_combine_vocab_shards(parts, y, V, opt, err_word=err)
+        dX = torch.zeros(wl.N, wl.H, dtype=torch.float32, device="cuda")
+        dWs = []
+        for b0, b1 in zip(bounds, bounds[1:]):
+            dxp, dws, _ = B.flce_backward_vocab_shard(X, W[b0:b1].contiguous(), y, b0, V, lse,
+                                                      nv, opt, err_word=err)
+            dX += dxp
+            dWs.append(dws)
+        dW = torch.cat(dWs)
+    else:
+        merged = path == "merged"
+        opt = B.make_options(-100, eps, backward_merge=merged, vocab_chunk=256 if merged else 0)
+        loss, lse, nv, dX, dW, _ = B.flce_fwd_bwd_ex(X, W, y, opt, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == B.FLCE_ERR_LABEL
+    got = dict(loss=float(loss.item()), lse=tensor_f64(lse), nv=int(nv.item()),
+               dX=tensor_f64(dX), dW=tensor_f64(dW), err=0)
+    f = O.forward(wl.x, wl.w, ref_labels, -100, eps)
+    b = O.backward(wl.x, wl.w, ref_labels, -100, eps)
+    assert got["nv"] == f.n_valid == wl.N - np.count_nonzero(ref_labels == -100)
+    assert rel_err(got["loss"], f.loss) <= LOSS_REL
+    assert np.max(np.abs(got["lse"] - f.lse)) <= LSE_ABS
+    assert rel_fro(got["dX"], b.dX) <= GRAD_REL_FRO
+    assert rel_fro(got["dW"], b.dW) <= GRAD_REL_FRO
+    assert np.all(got["dX"][bad] == 0.0)
+
+
 def test_large_logits_max_subtraction():
     """Logits far above 88.7 (where exp overflows fp32) stay finite and exact."""
     wl = I.make_workload(spec(N=256, H=64, V=900, n_ignore=8, w_std=1.0, x_std=4.0), seed=11)

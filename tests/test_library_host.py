@@ -41,8 +41,8 @@ def test_header_exports_all(L):
 
 
 def test_status_strings_and_version(L):
-    assert L.flce_abi_version() == 105
-    for s in range(7):
+    assert L.flce_abi_version() == 106
+    for s in range(8):
         assert L.flce_status_string(s).decode().startswith("FLCE_")
 
 
@@ -190,6 +190,7 @@ def test_options_struct_layout(L):
     assert o.struct_size == ctypes.sizeof(B.FlceOptions)
     assert (o.ignore_index, o.smoothing, o.z_loss, o.reduction, o.row_loss) == (-100, 0.0, 0.0, 0, None)
     assert (o.skip_ignored_blocks, o.grad_filter) == (0, 0.0)
+    assert (o.cta_pair, o.backward_merge, o.l2_hints, o.vocab_chunk) == (-1, -1, -1, -1)
     # a struct of another size is rejected before any CUDA call
     o.struct_size = 8
     P = ctypes.c_void_p
@@ -234,3 +235,101 @@ def test_plain_c_caller(L, tmp_path):
     assert int(out[2]) == B.flce_workspace_size(8192, 4096, 128256, B.FLCE_BF16, B.MODE_FWD_BWD)
     assert int(out[3]) == B.flce_vocab_chunk(8192, 4096, 128256)
     assert out[4].startswith("FLCE_ERR_ARG")
+
+
+def test_options_launch_settings_size_the_workspace(L):
+    """Launch settings in flce_options override the process-wide defaults for
+    one call, and flce_workspace_size_ex sizes with them; -1 fields and a
+    struct of the 1.05 size (no such fields) take the defaults."""
+    from linear_cross_entropy_logit_gb300 import binding as B
+    N, H, V = 8192, 4096, 128256
+    B.flce_set_vocab_chunk(0)
+    B.flce_set_backward_merge(False)
+    B.flce_set_cta_pair(True)
+    base = B.flce_workspace_size(N, H, V, B.FLCE_BF16, B.MODE_BWD)
+    o = B.make_options()
+    assert B.flce_workspace_size(N, H, V, B.FLCE_BF16, B.MODE_BWD, o) == base
+    assert B.flce_vocab_chunk(N, H, V, o) == 14592
+    merged = B.make_options(backward_merge=True)
+    assert B.flce_vocab_chunk(N, H, V, merged) == 8192
+    try:
+        B.flce_set_backward_merge(True)
+        assert B.flce_workspace_size(N, H, V, B.FLCE_BF16, B.MODE_BWD, merged) == \
+            B.flce_workspace_size(N, H, V, B.FLCE_BF16, B.MODE_BWD)
+        # an explicit 0 ignores the process-wide 1
+        off = B.make_options(backward_merge=False)
+        assert B.flce_workspace_size(N, H, V, B.FLCE_BF16, B.MODE_BWD, off) == base
+    finally:
+        B.flce_set_backward_merge(False)
+    chunk = B.make_options(vocab_chunk=2048)
+    assert B.flce_vocab_chunk(N, H, V, chunk) == 2048
+    assert B.flce_vocab_chunk(N, H, V) == 14592
+    # the 1.05 struct (no launch settings) is accepted and takes the defaults
+    old = B.make_options(vocab_chunk=2048)
+    old.struct_size = B.FlceOptions.cta_pair.offset
+    assert B.flce_workspace_size(N, H, V, B.FLCE_BF16, B.MODE_BWD, old) == base
+    # out-of-range settings are rejected (size 0)
+    for field, bad in (("cta_pair", 2), ("backward_merge", -2), ("l2_hints", 3),
+                       ("vocab_chunk", -5)):
+        o = B.make_options()
+        setattr(o, field, bad)
+        assert B.flce_workspace_size(N, H, V, B.FLCE_BF16, B.MODE_BWD, o) == 0, field
+
+
+def test_options_sizing_is_thread_safe():
+    """Two threads size workspaces with their own launch settings while a
+    third keeps flipping the process-wide defaults: each thread's sizes never
+    change, so a workspace sized this way always fits its call."""
+    import threading
+    from linear_cross_entropy_logit_gb300 import binding as B
+    N, H, V = 8192, 4096, 128256
+    mine = {"merged": B.make_options(backward_merge=True, cta_pair=True, vocab_chunk=0),
+            "plain": B.make_options(backward_merge=False, cta_pair=False, vocab_chunk=4096)}
+    want = {k: B.flce_workspace_size(N, H, V, B.FLCE_BF16, B.MODE_FWD_BWD, o)
+            for k, o in mine.items()}
+    assert want["merged"] != want["plain"]
+    stop = threading.Event()
+    bad = []
+
+    def flipper():
+        i = 0
+        while not stop.is_set():
+            B.flce_set_backward_merge(i % 2 == 0)
+            B.flce_set_cta_pair(i % 3 != 0)
+            B.flce_set_vocab_chunk((i % 4) * 1024)
+            i += 1
+
+    def sizer(key):
+        for _ in range(3000):
+            got = B.flce_workspace_size(N, H, V, B.FLCE_BF16, B.MODE_FWD_BWD, mine[key])
+            if got != want[key]:
+                bad.append((key, got))
+                return
+
+    t0 = threading.Thread(target=flipper)
+    ts = [threading.Thread(target=sizer, args=(k,)) for k in mine]
+    t0.start()
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    stop.set()
+    t0.join()
+    B.flce_set_backward_merge(False)
+    B.flce_set_cta_pair(True)
+    B.flce_set_vocab_chunk(0)
+    assert not bad
+
+
+def test_noalloc_rejects_misaligned_words(L):
+    """flce_forward_noalloc refuses 32-bit outputs that are not 4-byte aligned
+    on the host, before any CUDA call (no GPU needed)."""
+    from linear_cross_entropy_logit_gb300 import binding as B
+    P = ctypes.c_void_p
+    fake = 1 << 20
+    args = [P(fake), P(fake), P(fake), 64, 64, 1000, -100, 0.0, 0]
+    outs = [P(fake), P(fake), P(fake), P(fake)]  # loss, lse, valid_count, err_word
+    for i in range(4):
+        o = list(outs)
+        o[i] = P(fake + 2)
+        assert L.flce_forward_noalloc(*args, *o, None) == B.FLCE_ERR_ARG, i

@@ -42,6 +42,9 @@ CASES = [
     # ragged vocabulary and K tails
     (700, 256, 5000, 40, 0.1, 0, 21),
     (300, 136, 3000, 0, 0.0, 1, 22),
+    # partials of 501 vocabulary tiles x 4096 rows (32 MiB) do not fit the
+    # 16 MiB array one per tile: the call groups two tiles per partial
+    (4096, 256, 128256, 200, 0.0, 0, 24),
 ]
 
 
