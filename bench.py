@@ -72,9 +72,11 @@ def parse_args():
                     help="128x256 single-CTA tiles instead of 256x256 CTA-pair tiles")
     ap.add_argument("--clocks-dir", default=None,
                     help="directory for the raw nvidia-smi clock samples (default: temp dir)")
-    ap.add_argument("--merge", action="store_true",
-                    help="one merged dW(c) + dX(c) + dZ(c+1) backward launch per vocabulary "
-                         "chunk (two dZ buffers) instead of three launches")
+    ap.add_argument("--merge", type=int, nargs="?", const=1, default=None, choices=(0, 1, 2),
+                    help="backward layout: 0 three launches per vocabulary chunk; 1 (bare "
+                         "--merge) one merged dW(c) + dX(c) + dZ(c+1) launch per chunk (two dZ "
+                         "buffers); 2 dZ(c) alone, then one merged dW(c) + dX(c) launch; "
+                         "default: the library's default layout")
     return ap.parse_args()
 
 
@@ -307,10 +309,11 @@ def workload_spec(args):
 def kind_flops(B, N, H, V, args, merged):
     """Algorithmic FLOP per step of each profiled kernel kind.
 
-    Forward, dZ recompute, dW and dX each contract 2*N*V*H per step.  With
-    merged backward launches the dZ kind runs only chunk 0 of each backward
-    call (2*N*w0*H) and the merged kind the rest of the three backward
-    contractions (6*N*V*H minus that)."""
+    Forward, dZ recompute, dW and dX each contract 2*N*V*H per step.  With the
+    merged dW(c) + dX(c) + dZ(c+1) launches (merged = 1) the dZ kind runs only
+    chunk 0 of each backward call (2*N*w0*H) and the merged kind the rest of
+    the three backward contractions (6*N*V*H minus that); with merged dW(c) +
+    dX(c) launches (merged = 2) the merged kind does 4*N*V*H."""
     calls = [V]
     if args.vocab_shards > 1:
         P = args.vocab_shards
@@ -319,11 +322,22 @@ def kind_flops(B, N, H, V, args, merged):
     full = 2.0 * N * V * H
     out = {"fwd_logits_lse": full, "bwd_dz_recompute": full, "bwd_dw_gemm": full,
            "bwd_dx_gemm": full, "bwd_merged": 0.0}
-    if merged:
+    if merged == 2:
+        out["bwd_merged"] = 2.0 * full
+    elif merged:
         dz0 = sum(2.0 * N * min(B.flce_vocab_chunk(N, H, v), v) * H for v in calls)
         out["bwd_dz_recompute"] = dz0
         out["bwd_merged"] = 3.0 * full - dz0
     return out
+
+
+def backward_layout(mode, args) -> str:
+    """What the backward of this run launches per vocabulary chunk."""
+    if mode == 0 or args.single_cta or args.skip_ignored or args.grad_filter or args.l2_hints:
+        return "three launches per vocabulary chunk"
+    if mode == 1:
+        return "merged dW(c) + dX(c) + dZ(c+1) launch per vocabulary chunk (two dZ buffers)"
+    return "dZ(c) launch, then one merged dW(c) + dX(c) launch per vocabulary chunk"
 
 
 def workload_config(spec, chunk):
@@ -366,7 +380,9 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     B.flce_set_vocab_chunk(args.vocab_chunk)
     B.flce_set_l2_hints(args.l2_hints)
     B.flce_set_cta_pair(not args.single_cta)
-    B.flce_set_backward_merge(args.merge)
+    if args.merge is not None:
+        B.flce_set_backward_merge(args.merge)
+    merge_mode = B.flce_backward_merge()
     chunk = B.flce_vocab_chunk(N, H, V)
 
     def host_tensor(a):
@@ -600,7 +616,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
 
     # dominant kernel: largest share of the profiled device time
     kinds = {}
-    flops_kind = kind_flops(B, N, H, V, args, merged=prof["bwd_merged"][1] > 0)
+    flops_kind = kind_flops(B, N, H, V, args,
+                            merged=merge_mode if prof["bwd_merged"][1] > 0 else 0)
     total_prof_ms = sum(v[0] for v in prof.values()) or 1.0
     for name, (kms, n) in prof.items():
         if n == 0:
@@ -612,8 +629,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     dom = max(kinds, key=lambda k: kinds[k]["ms_total"]) if kinds else None
     roofline = None
     dense_default = not (args.skip_ignored or args.grad_filter or args.vocab_shards > 1 or
-                         args.shape or args.single_cta or args.l2_hints or args.merge or
-                         args.vocab_chunk)
+                         args.shape or args.single_cta or args.l2_hints or
+                         args.merge is not None or args.vocab_chunk)
     traffic = load_traffic(spec.name) if dense_default else None
     if dom:
         ach = kinds[dom]["tflops"]
@@ -638,7 +655,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     extra = {"workspace_bytes": ws.numel(),
              "workspace_vs_nxv_bf16": ws.numel() / (N * V * 2),
              "dz_chunk_bytes": N * chunk * 2,
-             "dz_buffers": 2 if (B.flce_backward_merge() and B.flce_cta_pair()) else 1,
+             "dz_buffers": 2 if (merge_mode == 1 and B.flce_cta_pair()) else 1,
              "peak_extra_device_bytes": peak_extra,
              "nxv_bf16_bytes": N * V * 2}
     line = {
@@ -650,10 +667,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                        l2="inputs larger than L2 (W alone is %.2f GB)" % (V * H * elem / 1e9),
                        parallelism=f"replicas x{world} (each rank its own batch, no collective)",
                        tiles="128x256 single CTA" if args.single_cta else "256x256 CTA pair",
-                       backward="merged dW(c) + dX(c) + dZ(c+1) launch per vocabulary chunk"
-                       if (args.merge and not (args.single_cta or args.skip_ignored
-                                               or args.grad_filter or args.l2_hints))
-                       else "three launches per vocabulary chunk",
+                       backward=backward_layout(merge_mode, args),
                        z_loss=args.z_loss,
                        skip_ignored_blocks=args.skip_ignored,
                        grad_filter=args.grad_filter or None,

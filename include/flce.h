@@ -113,19 +113,23 @@ int64_t flce_vocab_chunk(int64_t N, int64_t H, int64_t V);
 flce_status flce_set_cta_pair(int on);
 int flce_cta_pair(void);
 
-/* Merged backward launches, process-wide default (options field
- * backward_merge overrides it per call).  1: with CTA-pair tiles and none of
- * the optional features (skip_ignored_blocks, grad_filter, L2 hints), the
- * backward runs the dZ recompute of chunk 0 alone and then one launch per
- * vocabulary chunk c holding the dW and dX GEMMs of c and the dZ recompute of
- * c+1 in one tile list, so no GEMM ends on its own partial wave.  The
- * workspace then holds two N x Cv dZ buffers and one int per chunk.  0 (the
- * default): three launches per chunk, one dZ buffer.  Both give bit-identical
- * results for the same Cv.  Merging pays when Cv is small next to the tile
- * grid (measured on a GB300 at the Llama-3 shape: 6.8% faster steps at
- * Cv = 2048, 2.5% at 4096); at the default chunk width, and at equal dZ
- * memory, the three-launch backward was as fast or faster.  Set it before
- * sizing workspaces. */
+/* Backward layout, process-wide default (options field backward_merge
+ * overrides it per call).  With CTA-pair tiles and none of the optional
+ * features (skip_ignored_blocks, grad_filter, L2 hints):
+ *   0 (the default): per vocabulary chunk three launches -- the dZ
+ *     recompute, the dW GEMM, the dX GEMM -- and one dZ buffer;
+ *   1: the dZ recompute of chunk 0 alone, then one launch per chunk c holding
+ *     the dW and dX GEMMs of c and the dZ recompute of c+1 in one tile list,
+ *     so no GEMM ends on its own partial wave; the workspace then holds two
+ *     N x Cv dZ buffers;
+ *   2: per chunk the dZ recompute alone, then one launch of the dW and dX
+ *     GEMMs of that chunk from one tile list (one dZ buffer).
+ * Layouts 1 and 2 add one int per chunk to the workspace.  All give
+ * bit-identical results for the same Cv.  Layout 1 pays when Cv is small
+ * next to the tile grid (measured on a GB300 at the Llama-3 shape: 6.8%
+ * faster steps at Cv = 2048, 2.5% at 4096); at the default chunk width, and
+ * at equal dZ memory, the three-launch backward was as fast or faster.  Set
+ * it before sizing workspaces; other values return FLCE_ERR_ARG. */
 flce_status flce_set_backward_merge(int on);
 int flce_backward_merge(void);
 
@@ -208,7 +212,7 @@ flce_status flce_fwd_bwd(const void* X, const void* W, const int64_t* labels, in
  * the time of the call; any other value holds for this call only, so callers
  * in several threads can use different settings without racing):
  *   cta_pair        -1, 0 or 1: see flce_set_cta_pair
- *   backward_merge  -1, 0 or 1: see flce_set_backward_merge
+ *   backward_merge  -1, 0, 1 or 2: see flce_set_backward_merge
  *   l2_hints        -1, 0 or 1: see flce_set_l2_hints
  *   vocab_chunk     -1, 0 (automatic width) or a width in columns: see
  *                   flce_set_vocab_chunk

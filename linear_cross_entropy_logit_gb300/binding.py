@@ -243,14 +243,15 @@ def flce_cta_pair() -> bool:
     return bool(lib().flce_cta_pair())
 
 
-def flce_set_backward_merge(on: bool) -> None:
-    """1: one merged backward launch per vocabulary chunk (two dZ buffers);
-    0: three launches per chunk (default)."""
-    _check(lib().flce_set_backward_merge(int(bool(on))), "flce_set_backward_merge")
+def flce_set_backward_merge(mode) -> None:
+    """Backward layout: 0 three launches per chunk (default); 1 (or True) one
+    merged dW(c) + dX(c) + dZ(c+1) launch per chunk (two dZ buffers); 2 the dZ
+    recompute alone, then one merged dW(c) + dX(c) launch (one dZ buffer)."""
+    _check(lib().flce_set_backward_merge(int(mode)), "flce_set_backward_merge")
 
 
-def flce_backward_merge() -> bool:
-    return bool(lib().flce_backward_merge())
+def flce_backward_merge() -> int:
+    return int(lib().flce_backward_merge())
 
 
 def flce_vocab_chunk(N: int, H: int, V: int, options: Optional["FlceOptions"] = None) -> int:
@@ -275,7 +276,7 @@ def new_err_word(device) -> torch.Tensor:
 def make_options(ignore_index: int = -100, smoothing: float = 0.0, reduction: str = "mean",
                  z_loss: float = 0.0, row_loss=None, skip_ignored_blocks: bool = False,
                  grad_filter: float = 0.0, *, cta_pair: Optional[bool] = None,
-                 backward_merge: Optional[bool] = None, l2_hints: Optional[bool] = None,
+                 backward_merge: Optional[int] = None, l2_hints: Optional[bool] = None,
                  vocab_chunk: Optional[int] = None) -> FlceOptions:
     """An ``flce_options``; the launch settings left at None take the
     process-wide defaults at the time of each call."""
@@ -291,7 +292,7 @@ def make_options(ignore_index: int = -100, smoothing: float = 0.0, reduction: st
     if cta_pair is not None:
         o.cta_pair = int(bool(cta_pair))
     if backward_merge is not None:
-        o.backward_merge = int(bool(backward_merge))
+        o.backward_merge = int(backward_merge)
     if l2_hints is not None:
         o.l2_hints = int(bool(l2_hints))
     if vocab_chunk is not None:

@@ -57,6 +57,7 @@ struct FusedSeg {
   int n_blocks;    // ceil(n_size / 256)
   int m_fastest;   // 1: consecutive tiles walk row blocks; 0: walk column blocks
   int m_band;      // m_fastest: row blocks walked in bands of this many (0 = all)
+  int n_band;      // !m_fastest: column blocks walked in bands of this many (0 = all)
   int reduce_add;  // dW / dX: 1 = TMA reduce-add onto the output, 0 = overwrite
 };
 
@@ -116,6 +117,14 @@ __device__ __forceinline__ FusedTile fused_tile(const FusedParams& p, int t) {
       mb = l % s.m_blocks;
       nb = l / s.m_blocks;
     }
+  } else if (s.n_band > 0 && s.n_band < s.n_blocks) {
+    const int band_units = s.n_band * s.m_blocks;
+    const int band = l / band_units;
+    const int ub = l - band * band_units;
+    const int nb0 = band * s.n_band;
+    const int nbn = min(s.n_band, s.n_blocks - nb0);
+    nb = nb0 + ub % nbn;
+    mb = ub / nbn;
   } else {
     nb = l % s.n_blocks;
     mb = l / s.n_blocks;

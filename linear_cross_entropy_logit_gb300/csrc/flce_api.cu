@@ -63,13 +63,15 @@ std::atomic<int> g_l2_hints{0};
 // launches.
 struct Tuning {
   bool pair;           // 256 x 256 CTA-pair tiles (else 128 x 256 single-CTA)
-  bool merge;          // merged backward launches (only with pair tiles)
+  int merge;           // backward layout (pair tiles only): 0 three launches per chunk,
+                       // 1 dW(c) + dX(c) + dZ(c+1) merged (two dZ buffers),
+                       // 2 dW(c) + dX(c) merged after dZ(c) (one dZ buffer)
   bool l2_hints;       // evict_last policy on the re-read operand
   int64_t chunk_set;   // requested vocabulary chunk width (0 = automatic)
 };
 
 Tuning default_tuning() {
-  return Tuning{g_cta_pair.load() != 0, g_bwd_merge.load() != 0, g_l2_hints.load() != 0,
+  return Tuning{g_cta_pair.load() != 0, g_bwd_merge.load(), g_l2_hints.load() != 0,
                 g_vocab_chunk.load()};
 }
 
@@ -123,6 +125,7 @@ struct Plan {
   int64_t chunk;
   int n_chunks;
   int dz_bufs;  // 2 when the merged backward may run (dZ of chunk c+1 beside chunk c)
+  bool counters;  // one tile counter per chunk (merged launches of either layout)
   size_t off_scalars, off_blocks, off_partials, off_block_loss, off_block_valid, off_dz,
       off_dz2, off_counters, off_dxacc, off_xcast, off_wcast, off_mask_x, off_mask_w, total;
   // gradient-filter masks (sized for 128-row tiles, the smaller tile shape)
@@ -139,9 +142,11 @@ bool shape_ok(int64_t N, int64_t H, int64_t V) {
   return true;
 }
 
-// Whether backward calls may take the merged launches (CTA-pair tiles only);
-// their workspace then holds two dZ buffers.
-bool merge_planned(const Tuning& t) { return t.merge && t.pair; }
+// Whether backward calls may take the merged launches of dW(c), dX(c) and
+// dZ(c+1) (CTA-pair tiles only); their workspace then holds two dZ buffers.
+bool merge_planned(const Tuning& t) { return t.merge == 1 && t.pair; }
+// Whether backward calls may merge only dW(c) and dX(c) (one dZ buffer).
+bool merge_dwdx_planned(const Tuning& t) { return t.merge == 2 && t.pair; }
 int dz_buffers(const Tuning& t) { return merge_planned(t) ? 2 : 1; }
 
 // CTA pairs of a persistent launch on the current device (76 on a 152-SM
@@ -202,6 +207,7 @@ bool make_plan(int64_t N, int64_t H, int64_t V, flce_dtype dtype, int mode, cons
   p.chunk = auto_chunk(N, H, V, t);
   p.n_chunks = (int)ceil_div(V, p.chunk);
   p.dz_bufs = dz_buffers(t);
+  p.counters = merge_planned(t) || merge_dwdx_planned(t);
   const bool fwd = mode & FLCE_MODE_FWD;
   const bool bwd = mode & FLCE_MODE_BWD;
   size_t off = 0;
@@ -227,6 +233,8 @@ bool make_plan(int64_t N, int64_t H, int64_t V, flce_dtype dtype, int mode, cons
     if (p.dz_bufs == 2) {
       p.off_dz2 = off;
       off = align_up(off + (size_t)std::max<int64_t>(N, 1) * p.chunk * 2, kAlign);
+    }
+    if (p.counters) {
       p.off_counters = off;  // one tile counter per merged launch
       off = align_up(off + (size_t)p.n_chunks * sizeof(int), kAlign);
     }
@@ -271,10 +279,8 @@ bool plan_regions_ok(const Plan& p, flce_dtype dtype, int mode) {
   }
   if (mode & FLCE_MODE_BWD) {
     rs.push_back({p.off_dz, n1 * (size_t)p.chunk * 2});
-    if (p.dz_bufs == 2) {
-      rs.push_back({p.off_dz2, n1 * (size_t)p.chunk * 2});
-      rs.push_back({p.off_counters, (size_t)p.n_chunks * sizeof(int)});
-    }
+    if (p.dz_bufs == 2) rs.push_back({p.off_dz2, n1 * (size_t)p.chunk * 2});
+    if (p.counters) rs.push_back({p.off_counters, (size_t)p.n_chunks * sizeof(int)});
     if (dtype == FLCE_BF16) rs.push_back({p.off_dxacc, (size_t)p.N * p.H * 4});
     rs.push_back({p.off_mask_x, (size_t)ceil_div((int64_t)n1, BM) * p.mask_x_ld});
     rs.push_back({p.off_mask_w, (size_t)ceil_div(p.chunk, BM) * p.mask_w_ld});
@@ -782,90 +788,105 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
     p3.timeout_ns = kTimeoutNs;
     return p3;
   };
+  // One merged launch for chunk c: the dW(c) and dX(c) tiles, reading dZ(c)
+  // from `cur`, and -- when `next_buf` is set and a chunk c+1 exists -- the dZ
+  // recompute of chunk c+1 into `next_buf`, all from one tile list.
+  int* counters = reinterpret_cast<int*>(ws + pl.off_counters);
+  auto merged_launch = [&](int ci, const void* cur, void* next_buf) -> flce_status {
+    const int64_t v0 = (int64_t)ci * Cv;
+    const int64_t w = std::min(Cv, V - v0);
+    const bool next = next_buf != nullptr && ci + 1 < pl.n_chunks;
+    const int64_t v1 = v0 + Cv;
+    const int64_t w1 = next ? std::min(Cv, V - v1) : 0;
+    const void* Wc = Wb16 + v0 * H;
+    FusedMaps fm;
+    FLCE_TRY(map_mnmajor(&fm.a[kFusedDw], cur, w, N, Cv));
+    fm.b[kFusedDw] = tmX_mn;
+    FLCE_TRY(map_f32_out(&fm.out[kFusedDw], dW + v0 * H, H, w, H));
+    FLCE_TRY(map_kmajor(&fm.a[kFusedDx], cur, w, N, Cv, BM));
+    FLCE_TRY(map_mnmajor(&fm.b[kFusedDx], Wc, H, w, H));
+    fm.out[kFusedDx] = tmDxAcc;
+    fm.a[kFusedDz] = tmX_k;
+    if (next) {
+      FLCE_TRY(map_kmajor(&fm.b[kFusedDz], Wb16 + v1 * H, H, w1, H, b_box_rows(pair)));
+      FLCE_TRY(map_dz_store(&fm.out[kFusedDz], next_buf, w1, N, Cv));
+    } else {  // no dZ tiles: valid maps for the prefetch only
+      fm.b[kFusedDz] = tmX_k;
+      fm.out[kFusedDz] = tmX_k;
+    }
+    FusedSeg segs[3];
+    int n_seg = 0;
+    auto seg = [&](int kind, int m_size, int n_size, int k_size, int m_fastest, int m_band,
+                   int reduce_add) {
+      FusedSeg g{};
+      g.kind = kind;
+      g.m_size = m_size;
+      g.n_size = n_size;
+      g.k_size = k_size;
+      g.m_blocks = (int)ceil_div(m_size, 2 * BM);
+      g.n_blocks = (int)ceil_div(n_size, BN);
+      g.num_tiles = g.m_blocks * g.n_blocks;
+      g.m_fastest = m_fastest;
+      g.m_band = m_band;
+      g.reduce_add = reduce_add;
+      segs[n_seg++] = g;
+    };
+    // dX first among equals: its tiles hold a whole row block of dX_acc
+    seg(kFusedDx, (int)N, (int)H, (int)w, 0, 0, ci > 0 ? 1 : 0);
+    seg(kFusedDw, (int)w, (int)H, (int)N, 0, 0, accumulate ? 1 : 0);
+    if (next) seg(kFusedDz, (int)N, (int)w1, (int)H, 1, x_band(N, H, m_blocks_tok), 0);
+    // longest k-loop first, so the list ends on the shortest tiles
+    std::stable_sort(segs, segs + n_seg, [](const FusedSeg& a, const FusedSeg& b) {
+      return ceil_div(a.k_size, BK) > ceil_div(b.k_size, BK);
+    });
+    FusedParams fp{};
+    int first = 0;
+    for (int i = 0; i < n_seg; ++i) {
+      segs[i].first = first;
+      first += segs[i].num_tiles;
+      fp.seg[i] = segs[i];
+    }
+    fp.n_seg = n_seg;
+    fp.total_tiles = first;
+    fp.tile_counter = counters + ci;
+    fp.labels = c.labels;
+    fp.ignore_index = c.ignore_index;
+    fp.vocab = (int)c.vocab_total;
+    fp.col_base = (int)(c.vocab_offset + v1);
+    fp.col_limit = (int)w1;
+    fp.smoothing = c.smoothing;
+    fp.z_loss = c.z_loss;
+    fp.lse = lse;
+    fp.scale = scale;
+    fp.err_word = c.err_word;
+    fp.timeout_ns = kTimeoutNs;
+    return launch_fused(dev, sms, fm, fp, c.st);
+  };
+  // K3 alone for chunk ci: recompute Z[:, v0:v0+w] and write dZ into `buf`.
+  auto dz_launch = [&](int ci, void* buf, bool ext_kernel) -> flce_status {
+    const int64_t v0 = (int64_t)ci * Cv;
+    const int64_t w = std::min(Cv, V - v0);
+    CUtensorMap tmWc_k, tmDzSt;
+    FLCE_TRY(map_kmajor(&tmWc_k, Wb16 + v0 * H, H, w, H, b_box_rows(pair)));
+    FLCE_TRY(map_dz_store(&tmDzSt, buf, w, N, Cv));
+    return launch_tile<Epi::kDz, false, false>(pair, ext_kernel, dev, sms, tmX_k, tmWc_k, tmDzSt,
+                                               dz_params(v0, w), c.st, 1);
+  };
   if (pair && !ext && pl.dz_bufs == 2) {
     // Merged backward: dZ of chunk 0 alone, then per chunk c one launch of
     // dW(c), dX(c) and dZ(c+1), the dZ buffers taken in turn.
-    int* counters = reinterpret_cast<int*>(ws + pl.off_counters);
     FLCE_CUDA(cudaMemsetAsync(counters, 0, (size_t)pl.n_chunks * sizeof(int), c.st));
     void* dz_buf[2] = {ws + pl.off_dz, ws + pl.off_dz2};
-    {
-      const int64_t w0 = std::min(Cv, V);
-      CUtensorMap tmW0_k, tmDzSt0;
-      FLCE_TRY(map_kmajor(&tmW0_k, Wb16, H, w0, H, b_box_rows(pair)));
-      FLCE_TRY(map_dz_store(&tmDzSt0, dz_buf[0], w0, N, Cv));
-      FLCE_TRY((launch_tile<Epi::kDz, false, false>(pair, false, dev, sms, tmX_k, tmW0_k, tmDzSt0,
-                                                    dz_params(0, w0), c.st, 1)));
-    }
+    FLCE_TRY(dz_launch(0, dz_buf[0], false));
+    for (int ci = 0; ci < pl.n_chunks; ++ci)
+      FLCE_TRY(merged_launch(ci, dz_buf[ci & 1], dz_buf[(ci + 1) & 1]));
+  } else if (pair && !ext && pl.counters) {
+    // dW(c) and dX(c) merged: per chunk the dZ recompute alone, then one
+    // launch of both GEMMs that read it (one dZ buffer).
+    FLCE_CUDA(cudaMemsetAsync(counters, 0, (size_t)pl.n_chunks * sizeof(int), c.st));
     for (int ci = 0; ci < pl.n_chunks; ++ci) {
-      const int64_t v0 = (int64_t)ci * Cv;
-      const int64_t w = std::min(Cv, V - v0);
-      const bool next = ci + 1 < pl.n_chunks;
-      const int64_t v1 = v0 + Cv;
-      const int64_t w1 = next ? std::min(Cv, V - v1) : 0;
-      const void* cur = dz_buf[ci & 1];
-      const void* Wc = Wb16 + v0 * H;
-      FusedMaps fm;
-      FLCE_TRY(map_mnmajor(&fm.a[kFusedDw], cur, w, N, Cv));
-      fm.b[kFusedDw] = tmX_mn;
-      FLCE_TRY(map_f32_out(&fm.out[kFusedDw], dW + v0 * H, H, w, H));
-      FLCE_TRY(map_kmajor(&fm.a[kFusedDx], cur, w, N, Cv, BM));
-      FLCE_TRY(map_mnmajor(&fm.b[kFusedDx], Wc, H, w, H));
-      fm.out[kFusedDx] = tmDxAcc;
-      fm.a[kFusedDz] = tmX_k;
-      if (next) {
-        FLCE_TRY(map_kmajor(&fm.b[kFusedDz], Wb16 + v1 * H, H, w1, H, b_box_rows(pair)));
-        FLCE_TRY(map_dz_store(&fm.out[kFusedDz], dz_buf[(ci + 1) & 1], w1, N, Cv));
-      } else {  // no dZ tiles: valid maps for the prefetch only
-        fm.b[kFusedDz] = tmX_k;
-        fm.out[kFusedDz] = tmX_k;
-      }
-      FusedSeg segs[3];
-      int n_seg = 0;
-      auto seg = [&](int kind, int m_size, int n_size, int k_size, int m_fastest, int m_band,
-                     int reduce_add) {
-        FusedSeg g{};
-        g.kind = kind;
-        g.m_size = m_size;
-        g.n_size = n_size;
-        g.k_size = k_size;
-        g.m_blocks = (int)ceil_div(m_size, 2 * BM);
-        g.n_blocks = (int)ceil_div(n_size, BN);
-        g.num_tiles = g.m_blocks * g.n_blocks;
-        g.m_fastest = m_fastest;
-        g.m_band = m_band;
-        g.reduce_add = reduce_add;
-        segs[n_seg++] = g;
-      };
-      // dX first among equals: its tiles hold a whole row block of dX_acc
-      seg(kFusedDx, (int)N, (int)H, (int)w, 0, 0, ci > 0 ? 1 : 0);
-      seg(kFusedDw, (int)w, (int)H, (int)N, 0, 0, accumulate ? 1 : 0);
-      if (next) seg(kFusedDz, (int)N, (int)w1, (int)H, 1, x_band(N, H, m_blocks_tok), 0);
-      // longest k-loop first, so the list ends on the shortest tiles
-      std::stable_sort(segs, segs + n_seg, [](const FusedSeg& a, const FusedSeg& b) {
-        return ceil_div(a.k_size, BK) > ceil_div(b.k_size, BK);
-      });
-      FusedParams fp{};
-      int first = 0;
-      for (int i = 0; i < n_seg; ++i) {
-        segs[i].first = first;
-        first += segs[i].num_tiles;
-        fp.seg[i] = segs[i];
-      }
-      fp.n_seg = n_seg;
-      fp.total_tiles = first;
-      fp.tile_counter = counters + ci;
-      fp.labels = c.labels;
-      fp.ignore_index = c.ignore_index;
-      fp.vocab = (int)c.vocab_total;
-      fp.col_base = (int)(c.vocab_offset + v1);
-      fp.col_limit = (int)w1;
-      fp.smoothing = c.smoothing;
-      fp.z_loss = c.z_loss;
-      fp.lse = lse;
-      fp.scale = scale;
-      fp.err_word = c.err_word;
-      fp.timeout_ns = kTimeoutNs;
-      FLCE_TRY(launch_fused(dev, sms, fm, fp, c.st));
+      FLCE_TRY(dz_launch(ci, dz, false));
+      FLCE_TRY(merged_launch(ci, dz, nullptr));
     }
   } else {
     for (int ci = 0; ci < pl.n_chunks; ++ci) {
@@ -1030,7 +1051,8 @@ flce_status flce_set_cta_pair(int on) {
 int flce_cta_pair(void) { return g_cta_pair.load(); }
 
 flce_status flce_set_backward_merge(int on) {
-  g_bwd_merge.store(on != 0 ? 1 : 0);
+  if (on < 0 || on > 2) return FLCE_ERR_ARG;
+  g_bwd_merge.store(on);
   return FLCE_OK;
 }
 
@@ -1081,7 +1103,8 @@ bool options_ok(const flce_options* opt) {
   if (opt->struct_size == kOptionsV105Size) return true;
   if (opt->struct_size != sizeof(flce_options)) return false;
   auto tri = [](int v) { return v >= -1 && v <= 1; };
-  return tri(opt->cta_pair) && tri(opt->backward_merge) && tri(opt->l2_hints) &&
+  return tri(opt->cta_pair) && opt->backward_merge >= -1 && opt->backward_merge <= 2 &&
+         tri(opt->l2_hints) &&
          opt->vocab_chunk >= -1;
 }
 
@@ -1091,7 +1114,7 @@ Tuning resolve_tuning(const flce_options* opt) {
   Tuning t = default_tuning();
   if (!opt || opt->struct_size < sizeof(flce_options)) return t;
   if (opt->cta_pair >= 0) t.pair = opt->cta_pair != 0;
-  if (opt->backward_merge >= 0) t.merge = opt->backward_merge != 0;
+  if (opt->backward_merge >= 0) t.merge = opt->backward_merge;
   if (opt->l2_hints >= 0) t.l2_hints = opt->l2_hints != 0;
   if (opt->vocab_chunk >= 0) t.chunk_set = opt->vocab_chunk;
   return t;

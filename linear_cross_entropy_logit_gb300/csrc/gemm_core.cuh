@@ -86,6 +86,7 @@ struct GemmParams {
   int num_units;   // m_blocks * n_groups
   int m_fastest;   // 1: consecutive units walk row blocks (share B); 0: walk column groups
   int m_band;      // m_fastest: walk row blocks in bands of this many (0 = all at once)
+  int n_band;      // !m_fastest: walk column groups in bands of this many (0 = all at once)
   // kLse / kDz
   const int64_t* labels;  // per D row (token)
   long long ignore_index;
@@ -178,6 +179,16 @@ __device__ __forceinline__ void unit_coords(const GemmParams& p, const UnitSpace
       mb = u % us.m_blocks;
       g = u / us.m_blocks;
     }
+  } else if (p.n_band > 0 && p.n_band < p.n_groups) {
+    // bands of n_band column groups, each walked over all row blocks: the B
+    // operand of one band is re-read by every row block while it is in L2
+    const int band_units = p.n_band * us.m_blocks;
+    const int band = u / band_units;
+    const int ub = u - band * band_units;
+    const int g0 = band * p.n_band;
+    const int gn = min(p.n_band, p.n_groups - g0);
+    g = g0 + ub % gn;
+    mb = ub / gn;
   } else {
     g = u % p.n_groups;
     mb = u / p.n_groups;

@@ -51,6 +51,14 @@ def test_kind_flops_merged(bench):
     assert sum(f.values()) - f["bwd_dw_gemm"] - f["bwd_dx_gemm"] == pytest.approx(4.0 * full)
 
 
+def test_kind_flops_merged_dw_dx(bench):
+    N, H, V = 8192, 4096, 128256
+    f = bench.kind_flops(FakeLib(14592), N, H, V, args(), merged=2)
+    full = 2.0 * N * V * H
+    assert f["bwd_dz_recompute"] == f["fwd_logits_lse"] == full
+    assert f["bwd_merged"] == 2.0 * full
+
+
 def test_kind_flops_merged_vocab_shards(bench):
     """Each shard's backward runs its own chunk 0 alone."""
     N, H, V, cv = 1024, 512, 10000, 1024

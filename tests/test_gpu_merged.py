@@ -31,6 +31,8 @@ def _defaults():
 
 
 def _run(wl, merge, chunk, reduction="mean", grad=None, dW0=None, z_loss=0.0):
+    """merge: 0 three launches per chunk, 1 dW(c) + dX(c) + dZ(c+1) merged,
+    2 dZ(c) alone then dW(c) + dX(c) merged."""
     import torch
     from linear_cross_entropy_logit_gb300 import binding as B
     B.flce_set_backward_merge(merge)
@@ -68,18 +70,21 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("mode", [1, 2], ids=["dw_dx_dznext", "dw_dx"])
 @pytest.mark.parametrize("case", CASES, ids=[f"N{c[0]}-H{c[1]}-V{c[2]}-cv{c[6]}-{c[7]}"
                                               for c in CASES])
-def test_merged_equals_separate_launches(case):
+def test_merged_equals_separate_launches(case, mode):
     import torch
     N, H, V, n_ign, eps, zl, chunk, dt, seed = case
     spec = I.custom_spec("merged", N=N, H=H, V=V, dtype=dt, n_ignore=n_ign, smoothing=eps)
     wl = I.make_workload(spec, seed=seed)
-    a, pa = _run(wl, True, chunk, z_loss=zl)
-    b, pb = _run(wl, False, chunk, z_loss=zl)
+    a, pa = _run(wl, mode, chunk, z_loss=zl)
+    b, pb = _run(wl, 0, chunk, z_loss=zl)
     n_chunks = -(-V // chunk)
-    # the merged kernel ran once per chunk and no separate dW / dX launch did
-    assert pa["bwd_merged"][1] == n_chunks and pa["bwd_dz_recompute"][1] == 1
+    # the merged kernel ran once per chunk and no separate dW / dX launch did;
+    # the dZ recompute ran alone for chunk 0 (mode 1) or for every chunk (mode 2)
+    assert pa["bwd_merged"][1] == n_chunks
+    assert pa["bwd_dz_recompute"][1] == (1 if mode == 1 else n_chunks)
     assert pa["bwd_dw_gemm"][1] == 0 and pa["bwd_dx_gemm"][1] == 0
     assert pb["bwd_merged"][1] == 0 and pb["bwd_dw_gemm"][1] == n_chunks
     for k in ("loss", "lse", "nv", "dX", "dW"):
@@ -87,12 +92,13 @@ def test_merged_equals_separate_launches(case):
     assert float(a["dW"].abs().sum()) > 0 and float(a["dX"].float().abs().sum()) > 0
 
 
-def test_merged_sum_reduction_and_dw_accumulation():
+@pytest.mark.parametrize("mode", [1, 2], ids=["dw_dx_dznext", "dw_dx"])
+def test_merged_sum_reduction_and_dw_accumulation(mode):
     import torch
     spec = I.custom_spec("merged_acc", N=600, H=192, V=3300, dtype="bf16", n_ignore=25)
     wl = I.make_workload(spec, seed=36)
     dW0 = np.random.default_rng(7).standard_normal((3300, 192)).astype(np.float32)
-    a, _ = _run(wl, True, 512, reduction="sum", grad=0.37, dW0=dW0)
+    a, _ = _run(wl, mode, 512, reduction="sum", grad=0.37, dW0=dW0)
     b, _ = _run(wl, False, 512, reduction="sum", grad=0.37, dW0=dW0)
     for k in ("loss", "lse", "dX", "dW"):
         assert torch.equal(a[k], b[k]), k
@@ -113,7 +119,7 @@ def test_merged_vocab_shard_backward():
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     outs = []
-    for merge in (True, False):
+    for merge in (1, 2, 0):
         B.flce_set_backward_merge(merge)
         B.flce_set_vocab_chunk(512)
         assert B.flce_vocab_chunk(500, 256, 2200) == 512
@@ -121,7 +127,8 @@ def test_merged_vocab_shard_backward():
         torch.cuda.synchronize()
         assert int(e.item()) == 0
         outs.append((dxp.cpu(), dwp.cpu()))
-    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    for o in outs[1:]:
+        assert torch.equal(outs[0][0], o[0]) and torch.equal(outs[0][1], o[1])
 
 
 def test_optional_features_take_the_separate_launches():
@@ -173,5 +180,19 @@ def test_merged_equals_separate_launches_full_size():
     a, pa = _run(wl, True, 4096)
     b, pb = _run(wl, False, 4096)
     assert pa["bwd_merged"][1] == 32 and pb["bwd_dw_gemm"][1] == 32
+    for k in ("loss", "lse", "nv", "dX", "dW"):
+        assert torch.equal(a[k], b[k]), k
+
+
+@pytest.mark.slow
+def test_dw_dx_merged_equals_separate_launches_full_size():
+    """At the Llama-3 benchmark shape with the default chunk width (14592: 8
+    chunks and a last one of 11520): dZ(c) alone, then dW(c) and dX(c) from
+    one tile list of 912 + 512 tiles; same bits as three launches per chunk."""
+    import torch
+    wl = I.make_workload(I.CONFIGS["llama3_n8192"], seed=0)
+    a, pa = _run(wl, 2, 14592)
+    b, pb = _run(wl, 0, 14592)
+    assert pa["bwd_merged"][1] == 9 and pa["bwd_dz_recompute"][1] == 9
     for k in ("loss", "lse", "nv", "dX", "dW"):
         assert torch.equal(a[k], b[k]), k

@@ -23,7 +23,7 @@ def L():
 
 def _dz_buffers(B):
     """dZ buffers a backward workspace holds: two with merged launches."""
-    return 2 if (B.flce_backward_merge() and B.flce_cta_pair()) else 1
+    return 2 if (B.flce_backward_merge() == 1 and B.flce_cta_pair()) else 1
 
 
 def declared_functions():
