@@ -273,6 +273,25 @@ __device__ __forceinline__ void tmem_ld_wait_regs(uint32_t (&r)[32]) {
                : "memory");
 }
 
+// tcgen05.wait::ld with the 64 loaded registers as operands, so no use of
+// them can be scheduled before the wait.
+__device__ __forceinline__ void tmem_ld_wait_regs64(uint32_t (&r)[64]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+                 "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                 "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                 "+r"(r[30]), "+r"(r[31]), "+r"(r[32]), "+r"(r[33]), "+r"(r[34]), "+r"(r[35]),
+                 "+r"(r[36]), "+r"(r[37]), "+r"(r[38]), "+r"(r[39]), "+r"(r[40]), "+r"(r[41]),
+                 "+r"(r[42]), "+r"(r[43]), "+r"(r[44]), "+r"(r[45]), "+r"(r[46]), "+r"(r[47]),
+                 "+r"(r[48]), "+r"(r[49]), "+r"(r[50]), "+r"(r[51]), "+r"(r[52]), "+r"(r[53]),
+                 "+r"(r[54]), "+r"(r[55]), "+r"(r[56]), "+r"(r[57]), "+r"(r[58]), "+r"(r[59]),
+                 "+r"(r[60]), "+r"(r[61]), "+r"(r[62]), "+r"(r[63])
+               :
+               : "memory");
+}
+
 // One warp-uniform bounded wait: lane 0 polls, the result is broadcast.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtx& ctx,
                                           int lane) {
@@ -301,47 +320,56 @@ struct DzRow {
   float neg_lse2;  // -lse * log2(e)
   float eps_v;     // c * valid * eps / V
   float tgt;       // c * valid * (1 - eps)
+  float arg0;      // neg_lse2 + log2(pcoef) (-inf when pcoef = 0): pcoef * p = exp2(z log2 e + arg0)
 };
 
 __device__ __forceinline__ DzRow dz_row(bool valid, float lse_r, float c, float eps, float z_loss,
                                         int vocab) {
   const float coef = valid ? c : 0.f;
-  return {coef * fmaf(2.f * z_loss, lse_r, 1.f), -lse_r * LOG2E, coef * eps / (float)vocab,
-          coef * (1.f - eps)};
+  const float pcoef = coef * fmaf(2.f * z_loss, lse_r, 1.f);
+  const float neg_lse2 = -lse_r * LOG2E;
+  return {pcoef, neg_lse2, coef * eps / (float)vocab, coef * (1.f - eps),
+          neg_lse2 + __log2f(pcoef)};
 }
 
 // dZ of one 64-column slice of this thread's row: TMEM columns taddr .. +63 in,
 // 32 packed bf16 pairs out; `off` = label - first column of the slice.
 // Returns the largest probability of the slice when PMAX (gradient filtering).
+// All 32 lanes of the warp must call it together (the target check is a
+// warp vote: only a slice holding some lane's target walks the select chain).
 template <bool PMAX>
 __device__ __forceinline__ float dz_slice(uint32_t taddr, const DzRow& d, long long off,
                                           uint32_t (&w)[32]) {
-  uint32_t r0[32], r1[32];
-  tmem_ld_32x32b_x32(taddr, r0);
-  tmem_ld_32x32b_x32(taddr + 32, r1);
-  tmem_ld_wait_regs(r0);
-  tmem_ld_wait_regs(r1);
-  float pmax = 0.f;
+  uint32_t r[64];
+  tmem_ld_32x32b_x64(taddr, r);
+  tmem_ld_wait_regs64(r);
+  float pm[2] = {0.f, 0.f};
+  // Without smoothing and with a non-negative scale on every lane's row the
+  // scale folds into the exponent: pcoef * p = exp2(z log2 e + arg0), one FFMA
+  // and one exp2 per element (warp-uniform choice).
+  if (!PMAX && __all_sync(0xffffffffu, d.eps_v == 0.f && d.pcoef >= 0.f)) {
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    const float za = __uint_as_float(r0[j]);
-    const float zb = __uint_as_float(r1[j]);
-    const float pa = ex2_approx(fmaf(za, LOG2E, d.neg_lse2));
-    const float pb = ex2_approx(fmaf(zb, LOG2E, d.neg_lse2));
-    if constexpr (PMAX) pmax = fmaxf(pmax, fmaxf(pa, pb));
-    float da = fmaf(d.pcoef, pa, -d.eps_v);
-    float db = fmaf(d.pcoef, pb, -d.eps_v);
-    if (off == j) da -= d.tgt;
-    if (off == j + 32) db -= d.tgt;
-    r0[j] = __float_as_uint(da);
-    r1[j] = __float_as_uint(db);
+    for (int j = 0; j < 64; ++j)
+      r[j] = __float_as_uint(ex2_approx(fmaf(__uint_as_float(r[j]), LOG2E, d.arg0)));
+  } else {
+#pragma unroll
+    for (int j = 0; j < 64; ++j) {
+      const float pj = ex2_approx(fmaf(__uint_as_float(r[j]), LOG2E, d.neg_lse2));
+      if constexpr (PMAX) pm[j & 1] = fmaxf(pm[j & 1], pj);
+      r[j] = __float_as_uint(fmaf(d.pcoef, pj, -d.eps_v));
+    }
+  }
+  const bool mine = off >= 0 && off < 64;
+  if (__any_sync(0xffffffffu, mine)) {
+    const int offi = mine ? (int)off : -1;
+#pragma unroll
+    for (int j = 0; j < 64; ++j)
+      r[j] = (j == offi) ? __float_as_uint(__uint_as_float(r[j]) - d.tgt) : r[j];
   }
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    w[j] = pack_bf16x2(__uint_as_float(r0[2 * j]), __uint_as_float(r0[2 * j + 1]));
-    w[16 + j] = pack_bf16x2(__uint_as_float(r1[2 * j]), __uint_as_float(r1[2 * j + 1]));
-  }
-  return pmax;
+  for (int j = 0; j < 32; ++j)
+    w[j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+  return fmaxf(pm[0], pm[1]);
 }
 
 // One warp writes its 32 rows x 128 bytes (one row per lane) through a
@@ -682,41 +710,58 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
         const uint32_t taddr = lane_base + acc * BN;
 
         if constexpr (EPI == Epi::kLse) {
+          // 64-column slices.  The epilogue runs beside the next tile's MMAs
+          // and competes with them for the SM, so it is kept lean: a tile
+          // wholly inside the vocabulary skips the per-column range check,
+          // the exponent argument is one FFMA, the max and sum run as four
+          // independent chains, and the target-logit gather only runs for a
+          // slice that holds some lane's target (a warp vote).
+          const int tile_c0 = nb * BN;
+          const bool full_tile = tile_c0 + BN <= p.col_limit;  // warp-uniform
 #pragma unroll 1
-          for (int ch = 0; ch < BN / 32; ++ch) {
-            const int c0 = nb * BN + ch * 32;
+          for (int sl = 0; sl < BN / 64; ++sl) {
+            const int c0 = tile_c0 + sl * 64;
             const int nvalid = p.col_limit - c0;  // warp-uniform
             if (nvalid <= 0) break;
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(taddr + ch * 32, r);
-            tmem_ld_wait_regs(r);
-            float t[32];
-            float cmax = -INFINITY;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float z = __uint_as_float(r[j]);
-              t[j] = (j < nvalid) ? z * LOG2E : -INFINITY;
-              cmax = fmaxf(cmax, t[j]);
-            }
-            if (cmax > m2) {
-              ssum *= ex2_approx(m2 - cmax);
-              m2 = cmax;
-            }
-            float part = 0.f;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) part += ex2_approx(t[j] - m2);
-            ssum += part;
+            uint32_t r[64];
+            tmem_ld_32x32b_x64(taddr + sl * 64, r);
+            tmem_ld_wait_regs64(r);
             if (p.smoothing != 0.f) {
-              float zs = 0.f;
+              float zs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-              for (int j = 0; j < 32; ++j) zs += (j < nvalid) ? __uint_as_float(r[j]) : 0.f;
-              zsum += zs;
+              for (int j = 0; j < 64; ++j)
+                zs[j & 3] += (full_tile || j < nvalid) ? __uint_as_float(r[j]) : 0.f;
+              zsum += (zs[0] + zs[1]) + (zs[2] + zs[3]);
             }
             // target logit: a select chain (no dynamic register indexing)
             const long long off = lab_rel - c0;
-            const int offi = (off >= 0 && off < 32 && off < nvalid) ? (int)off : -1;
+            const bool mine = off >= 0 && off < 64 && off < nvalid;
+            if (__any_sync(0xffffffffu, mine)) {
+              const int offi = mine ? (int)off : -1;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) zy = (j == offi) ? __uint_as_float(r[j]) : zy;
+              for (int j = 0; j < 64; ++j) zy = (j == offi) ? __uint_as_float(r[j]) : zy;
+            }
+            if (!full_tile) {
+#pragma unroll
+              for (int j = 0; j < 64; ++j)
+                if (j >= nvalid) r[j] = __float_as_uint(-INFINITY);
+            }
+            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int j = 0; j < 64; j += 2)
+              mx[(j >> 1) & 3] =
+                  fmax3(mx[(j >> 1) & 3], __uint_as_float(r[j]), __uint_as_float(r[j + 1]));
+            // running max in units of log2 (scaling by log2(e) > 0 keeps the order)
+            const float cm2 = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * LOG2E;
+            if (cm2 > m2) {
+              ssum *= ex2_approx(m2 - cm2);
+              m2 = cm2;
+            }
+            float ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int j = 0; j < 64; ++j)
+              ps[j & 3] += ex2_approx(fmaf(__uint_as_float(r[j]), LOG2E, -m2));
+            ssum += (ps[0] + ps[1]) + (ps[2] + ps[3]);
           }
         } else if constexpr (EPI == Epi::kDz) {
 #pragma unroll 1
