@@ -68,6 +68,9 @@ def parse_args():
                     help="skip token blocks whose labels are all ignore_index")
     ap.add_argument("--z-loss", type=float, default=0.0,
                     help="z-loss weight alpha (adds alpha * lse^2 per valid token)")
+    ap.add_argument("--multicast", type=int, default=None, choices=(0, 1),
+                    help="operand multicast between CTA pairs in 4-CTA clusters (1) or plain "
+                         "CTA pairs (0); default: the library's default")
     ap.add_argument("--single-cta", action="store_true",
                     help="128x256 single-CTA tiles instead of 256x256 CTA-pair tiles")
     ap.add_argument("--clocks-dir", default=None,
@@ -380,6 +383,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     B.flce_set_vocab_chunk(args.vocab_chunk)
     B.flce_set_l2_hints(args.l2_hints)
     B.flce_set_cta_pair(not args.single_cta)
+    if args.multicast is not None:
+        B.flce_set_cluster_multicast(bool(args.multicast))
     if args.merge is not None:
         B.flce_set_backward_merge(args.merge)
     merge_mode = B.flce_backward_merge()
@@ -630,7 +635,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     roofline = None
     dense_default = not (args.skip_ignored or args.grad_filter or args.vocab_shards > 1 or
                          args.shape or args.single_cta or args.l2_hints or
-                         args.merge is not None or args.vocab_chunk)
+                         args.merge is not None or args.vocab_chunk or
+                         args.multicast is not None)
     traffic = load_traffic(spec.name) if dense_default else None
     if dom:
         ach = kinds[dom]["tflops"]
@@ -667,6 +673,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                        l2="inputs larger than L2 (W alone is %.2f GB)" % (V * H * elem / 1e9),
                        parallelism=f"replicas x{world} (each rank its own batch, no collective)",
                        tiles="128x256 single CTA" if args.single_cta else "256x256 CTA pair",
+                       cluster_multicast=(not args.single_cta) and B.flce_cluster_multicast(),
                        backward=backward_layout(merge_mode, args),
                        z_loss=args.z_loss,
                        skip_ignored_blocks=args.skip_ignored,

@@ -113,6 +113,20 @@ int64_t flce_vocab_chunk(int64_t N, int64_t H, int64_t V);
 flce_status flce_set_cta_pair(int on);
 int flce_cta_pair(void);
 
+/* Operand multicast between CTA pairs, process-wide default (options field
+ * cluster_multicast overrides it per call).  1 (the default): a CTA-pair GEMM
+ * launch of the plain kernels (none of skip_ignored_blocks, grad_filter, L2
+ * hints) whose tiles pair up -- an even number of row blocks sharing each
+ * column block, or of column blocks sharing each row block -- is launched
+ * with 4-CTA clusters preferred; the two pairs of a 4-CTA cluster compute two
+ * such tiles in step and multicast the operand they share (TMA .multicast),
+ * so each loads a quarter less from L2.  The hardware may group any four CTAs
+ * as two 2-CTA clusters instead; those compute the same tiles without
+ * multicast.  0: plain CTA pairs.  Results are bit-identical either way.
+ * Not used by the merged backward launches. */
+flce_status flce_set_cluster_multicast(int on);
+int flce_cluster_multicast(void);
+
 /* Backward layout, process-wide default (options field backward_merge
  * overrides it per call).  With CTA-pair tiles and none of the optional
  * features (skip_ignored_blocks, grad_filter, L2 hints):
@@ -216,6 +230,7 @@ flce_status flce_fwd_bwd(const void* X, const void* W, const int64_t* labels, in
  *   l2_hints        -1, 0 or 1: see flce_set_l2_hints
  *   vocab_chunk     -1, 0 (automatic width) or a width in columns: see
  *                   flce_set_vocab_chunk
+ *   cluster_multicast -1, 0 or 1: see flce_set_cluster_multicast
  * The workspace of a call must be sized with the same settings:
  * flce_workspace_size_ex with the same options.  A struct from a caller built
  * against ABI 1.05 (struct_size = offsetof(flce_options, cta_pair)) is
@@ -233,6 +248,7 @@ typedef struct flce_options {
   int backward_merge;
   int l2_hints;
   int64_t vocab_chunk;
+  int cluster_multicast;
 } flce_options;
 
 void flce_options_init(flce_options* opt);
@@ -362,6 +378,11 @@ int flce_abi_version(void);
  * leaving the CUDA context usable. */
 flce_status flce_debug_wait_timeout(int32_t* err_word, uint64_t timeout_ns, int32_t* waited_us,
                                     void* stream);
+
+/* TEST-ONLY: how many GEMM launches of the last call on this thread were made
+ * with 4-CTA clusters preferred (the operand-multicast walk of
+ * flce_set_cluster_multicast). */
+int flce_debug_last_multicast_launches(void);
 
 /* TEST-ONLY: the library's tcgen05 GEMM core without a loss epilogue.
  * D (M x Nn fp32, device, row-major) = A * B^T, or += when accumulate != 0,

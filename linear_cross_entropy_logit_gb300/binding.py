@@ -44,7 +44,8 @@ EXPORTED = (
     "flce_forward_ex", "flce_backward_ex", "flce_fwd_bwd_ex", "flce_forward_vocab_shard",
     "flce_combine_workspace_size", "flce_combine_vocab_shards", "flce_backward_vocab_shard",
     "flce_debug_wait_timeout", "flce_set_backward_merge", "flce_backward_merge",
-    "flce_workspace_size_ex", "flce_vocab_chunk_ex",
+    "flce_workspace_size_ex", "flce_vocab_chunk_ex", "flce_set_cluster_multicast",
+    "flce_cluster_multicast", "flce_debug_last_multicast_launches",
 )
 
 PROFILE_KINDS = ("fwd_logits_lse", "bwd_dz_recompute", "bwd_dw_gemm", "bwd_dx_gemm",
@@ -60,7 +61,8 @@ class FlceOptions(ctypes.Structure):
                 ("reduction", ctypes.c_int), ("row_loss", ctypes.c_void_p),
                 ("skip_ignored_blocks", ctypes.c_int), ("grad_filter", ctypes.c_float),
                 ("cta_pair", ctypes.c_int), ("backward_merge", ctypes.c_int),
-                ("l2_hints", ctypes.c_int), ("vocab_chunk", ctypes.c_int64)]
+                ("l2_hints", ctypes.c_int), ("vocab_chunk", ctypes.c_int64),
+                ("cluster_multicast", ctypes.c_int)]
 
 
 class FlceError(RuntimeError):
@@ -168,6 +170,12 @@ def load(path: str) -> ctypes.CDLL:
     L.flce_workspace_size_ex.restype = SZ
     L.flce_vocab_chunk_ex.argtypes = [I64, I64, I64, OPT]
     L.flce_vocab_chunk_ex.restype = I64
+    L.flce_set_cluster_multicast.argtypes = [I32]
+    L.flce_set_cluster_multicast.restype = I32
+    L.flce_cluster_multicast.argtypes = []
+    L.flce_cluster_multicast.restype = I32
+    L.flce_debug_last_multicast_launches.argtypes = []
+    L.flce_debug_last_multicast_launches.restype = I32
     return L
 
 
@@ -243,6 +251,16 @@ def flce_cta_pair() -> bool:
     return bool(lib().flce_cta_pair())
 
 
+def flce_set_cluster_multicast(on: bool) -> None:
+    """1: pair launches whose tiles pair up take 4-CTA clusters with operand
+    multicast (default); 0: plain CTA pairs.  Bit-identical results."""
+    _check(lib().flce_set_cluster_multicast(int(bool(on))), "flce_set_cluster_multicast")
+
+
+def flce_cluster_multicast() -> bool:
+    return bool(lib().flce_cluster_multicast())
+
+
 def flce_set_backward_merge(mode) -> None:
     """Backward layout: 0 three launches per chunk (default); 1 (or True) one
     merged dW(c) + dX(c) + dZ(c+1) launch per chunk (two dZ buffers); 2 the dZ
@@ -277,7 +295,8 @@ def make_options(ignore_index: int = -100, smoothing: float = 0.0, reduction: st
                  z_loss: float = 0.0, row_loss=None, skip_ignored_blocks: bool = False,
                  grad_filter: float = 0.0, *, cta_pair: Optional[bool] = None,
                  backward_merge: Optional[int] = None, l2_hints: Optional[bool] = None,
-                 vocab_chunk: Optional[int] = None) -> FlceOptions:
+                 vocab_chunk: Optional[int] = None,
+                 cluster_multicast: Optional[bool] = None) -> FlceOptions:
     """An ``flce_options``; the launch settings left at None take the
     process-wide defaults at the time of each call."""
     o = FlceOptions()
@@ -297,6 +316,8 @@ def make_options(ignore_index: int = -100, smoothing: float = 0.0, reduction: st
         o.l2_hints = int(bool(l2_hints))
     if vocab_chunk is not None:
         o.vocab_chunk = int(vocab_chunk)
+    if cluster_multicast is not None:
+        o.cluster_multicast = int(bool(cluster_multicast))
     return o
 
 
@@ -548,6 +569,11 @@ def flce_forward_noalloc(X, W, labels, ignore_index: int = -100, smoothing: floa
 
 def last_launch_count() -> int:
     return int(lib().flce_last_launch_count())
+
+
+def last_multicast_launches() -> int:
+    """Test-only: launches of the last call made with the operand-multicast walk."""
+    return int(lib().flce_debug_last_multicast_launches())
 
 
 def flce_profile_enable(on: bool) -> None:

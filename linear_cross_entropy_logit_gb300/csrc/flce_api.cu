@@ -51,12 +51,14 @@ constexpr size_t kAlign = 256;
 
 thread_local std::string g_last_cuda_error;
 thread_local int g_launches = 0;
+thread_local int g_quad_launches = 0;  // launches of the last call that took the QUAD walk
 // Process-wide defaults of the launch settings; a call whose options set a
 // field itself does not read the matching default.
 std::atomic<int64_t> g_vocab_chunk{0};
 std::atomic<int> g_cta_pair{1};
 std::atomic<int> g_bwd_merge{0};
 std::atomic<int> g_l2_hints{0};
+std::atomic<int> g_cluster_mcast{1};
 
 // Launch settings of one call, resolved once at its entry from its options
 // and the process-wide defaults, and used for both the workspace plan and the
@@ -68,11 +70,12 @@ struct Tuning {
                        // 2 dW(c) + dX(c) merged after dZ(c) (one dZ buffer)
   bool l2_hints;       // evict_last policy on the re-read operand
   int64_t chunk_set;   // requested vocabulary chunk width (0 = automatic)
+  bool mcast;          // pair launches may take 4-CTA clusters with operand multicast
 };
 
 Tuning default_tuning() {
   return Tuning{g_cta_pair.load() != 0, g_bwd_merge.load(), g_l2_hints.load() != 0,
-                g_vocab_chunk.load()};
+                g_vocab_chunk.load(), g_cluster_mcast.load() != 0};
 }
 
 // Optional per-kernel timing: CUDA events recorded on the caller's stream
@@ -456,11 +459,93 @@ flce_status launch_gemm(int dev, int num_sms, const CUtensorMap& a, const CUtens
   return FLCE_OK;
 }
 
-// Run-time choice between the 1-CTA (128 x 256) and CTA-pair (256 x 256) kernels.
+// The walk of a CTA-pair launch: plain pairs (2-CTA clusters), or the QUAD
+// walk (4-CTA clusters preferred, the two pairs of a cluster multicasting the
+// operand their tiles share; see gemm_core.cuh).
+struct Walk {
+  bool quad = false;
+  bool share_b = false;  // QUAD: the pairs share B (differ in row block), else A
+};
+
+// QUAD needs whole groups of two pairs whose units pair up exactly: units
+// 2v and 2v+1 must differ only in the row block (share B) or only in the
+// column group (share A, group length 1), and every unit needs its partner.
+Walk pick_walk(const Tuning& t, bool pair, bool ext, const GemmParams& p) {
+  Walk w;
+  if (!pair || ext || !t.mcast || p.num_units < 4 || p.num_units % 2 != 0) return w;
+  if (p.m_fastest) {
+    const bool banded = p.m_band > 0 && p.m_band < p.m_blocks;
+    if (p.m_blocks % 2 != 0 || (banded && p.m_band % 2 != 0)) return w;
+    w.quad = w.share_b = true;
+  } else if (p.group_len == 1 && p.n_groups % 2 == 0) {
+    w.quad = true;
+  } else if (p.m_blocks % 2 == 0) {
+    w.quad = w.share_b = true;
+  }
+  return w;
+}
+
+// Rows of a K-major operand box: QUAD loads every operand half as two 64-row
+// boxes; pairs load their 128 rows of A and of B in one box each, single CTAs
+// 128 rows of A and 256 of B.
+uint32_t a_box_rows(const Walk& w) { return w.quad ? 64 : BM; }
+uint32_t b_box_rows(bool pair, const Walk& w) { return w.quad ? 64 : (pair ? BN / 2 : BN); }
+
+template <Epi EPI, bool A_MN, bool B_MN, bool SHARE_B>
+flce_status launch_quad(int dev, int num_sms, const CUtensorMap& a, const CUtensorMap& b,
+                        const CUtensorMap& out, const GemmParams& p, cudaStream_t st,
+                        int prof_kind) {
+  auto kern = gemm_quad_kernel<EPI, A_MN, B_MN, kPairStages, SHARE_B>;
+  constexpr int smem = gemm_smem_bytes<EPI, kPairStages, true, false>();
+  static KernelSetup setup[kMaxDevices];
+  setup_kernel(setup[dev], kern, smem, false, num_sms);
+  if (setup[dev].err != cudaSuccess) return cuda_fail(setup[dev].err, setup[dev].what);
+  if (p.num_units <= 0) return FLCE_OK;
+  // An even number of pairs, so that the two pairs of every group of four
+  // CTAs take partner units; the hardware groups each four into one 4-CTA
+  // cluster where it can, else into two 2-CTA clusters (no multicast).
+  const int pairs = std::min(p.num_units, num_sms / 2) & ~1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  at[1].id = cudaLaunchAttributePreferredClusterDimension;
+  at[1].val.preferredClusterDim.x = 4;
+  at[1].val.preferredClusterDim.y = 1;
+  at[1].val.preferredClusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 2;
+  ProfRec rec{prof_kind, nullptr, nullptr};
+  if (g_prof_on && prof_kind >= 0) {
+    rec.start = prof_event();
+    rec.stop = prof_event();
+    if (rec.start && rec.stop) FLCE_CUDA(cudaEventRecord(rec.start, st));
+  }
+  FLCE_CUDA(cudaLaunchKernelEx(&cfg, kern, a, b, out, p));
+  ++g_launches;
+  ++g_quad_launches;
+  if (rec.start && rec.stop) {
+    FLCE_CUDA(cudaEventRecord(rec.stop, st));
+    g_prof_pending.push_back(rec);
+  }
+  return FLCE_OK;
+}
+
+// Run-time choice between the 1-CTA (128 x 256), CTA-pair (256 x 256) and
+// QUAD kernels.
 template <Epi EPI, bool A_MN, bool B_MN>
-flce_status launch_tile(bool pair, bool ext, int dev, int num_sms, const CUtensorMap& a,
-                        const CUtensorMap& b, const CUtensorMap& out, const GemmParams& p,
-                        cudaStream_t st, int prof_kind = -1) {
+flce_status launch_tile(bool pair, bool ext, const Walk& w, int dev, int num_sms,
+                        const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out,
+                        const GemmParams& p, cudaStream_t st, int prof_kind = -1) {
+  if (w.quad)
+    return w.share_b ? launch_quad<EPI, A_MN, B_MN, true>(dev, num_sms, a, b, out, p, st, prof_kind)
+                     : launch_quad<EPI, A_MN, B_MN, false>(dev, num_sms, a, b, out, p, st, prof_kind);
   if (ext)
     return pair ? launch_gemm<EPI, A_MN, B_MN, true, true>(dev, num_sms, a, b, out, p, st, prof_kind)
                 : launch_gemm<EPI, A_MN, B_MN, false, true>(dev, num_sms, a, b, out, p, st, prof_kind);
@@ -649,9 +734,6 @@ flce_status run_forward(const Common& c, const Plan& pl, int dev, int sms, const
     const bool pair = c.tun.pair;
     SkipLists sk;
     FLCE_TRY(build_skip_lists(c, pl, pair, &sk));
-    CUtensorMap tmX, tmW;
-    FLCE_TRY(map_kmajor(&tmX, Xb, c.H, c.N, c.H, BM));
-    FLCE_TRY(map_kmajor(&tmW, Wb, c.H, c.V, c.H, b_box_rows(pair)));
     GemmParams p{};
     p.m_size = (int)c.N;
     p.n_size = (int)c.V;
@@ -678,7 +760,12 @@ flce_status run_forward(const Common& c, const Plan& pl, int dev, int sms, const
     p.list_cap = pl.n_blocks128;
     p.err_word = c.err_word;
     p.timeout_ns = kTimeoutNs;
-    FLCE_TRY((launch_tile<Epi::kLse, false, false>(pair, ext_features(c), dev, sms, tmX, tmW, tmX, p,
+    const bool ext = ext_features(c);
+    const Walk walk = pick_walk(c.tun, pair, ext, p);
+    CUtensorMap tmX, tmW;
+    FLCE_TRY(map_kmajor(&tmX, Xb, c.H, c.N, c.H, a_box_rows(walk)));
+    FLCE_TRY(map_kmajor(&tmW, Wb, c.H, c.V, c.H, b_box_rows(pair, walk)));
+    FLCE_TRY((launch_tile<Epi::kLse, false, false>(pair, ext, walk, dev, sms, tmX, tmW, tmX, p,
                                                   c.st, 0)));
     if (shard_out) {
       // vocabulary shard: one merged partial per row, no loss yet
@@ -722,8 +809,11 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
                       : static_cast<float*>(dX);
   const auto* Wb16 = static_cast<const uint16_t*>(Wb);
 
-  CUtensorMap tmX_k, tmX_mn, tmDxAcc;
+  // X as the K-major A operand of the dZ recompute: 128-row boxes (pairs, the
+  // merged launches) or 64-row boxes (QUAD walks)
+  CUtensorMap tmX_k, tmX_k64, tmX_mn, tmDxAcc;
   FLCE_TRY(map_kmajor(&tmX_k, Xb, H, N, H, BM));
+  FLCE_TRY(map_kmajor(&tmX_k64, Xb, H, N, H, 64));
   FLCE_TRY(map_mnmajor(&tmX_mn, Xb, H, N, H));
   FLCE_TRY(map_f32_out(&tmDxAcc, dx_acc, H, N, H));
 
@@ -866,11 +956,14 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
   auto dz_launch = [&](int ci, void* buf, bool ext_kernel) -> flce_status {
     const int64_t v0 = (int64_t)ci * Cv;
     const int64_t w = std::min(Cv, V - v0);
+    const GemmParams p3 = dz_params(v0, w);
+    const Walk w3 = pick_walk(c.tun, pair, ext_kernel, p3);
     CUtensorMap tmWc_k, tmDzSt;
-    FLCE_TRY(map_kmajor(&tmWc_k, Wb16 + v0 * H, H, w, H, b_box_rows(pair)));
+    FLCE_TRY(map_kmajor(&tmWc_k, Wb16 + v0 * H, H, w, H, b_box_rows(pair, w3)));
     FLCE_TRY(map_dz_store(&tmDzSt, buf, w, N, Cv));
-    return launch_tile<Epi::kDz, false, false>(pair, ext_kernel, dev, sms, tmX_k, tmWc_k, tmDzSt,
-                                               dz_params(v0, w), c.st, 1);
+    return launch_tile<Epi::kDz, false, false>(pair, ext_kernel, w3, dev, sms,
+                                               w3.quad ? tmX_k64 : tmX_k, tmWc_k, tmDzSt, p3,
+                                               c.st, 1);
   };
   if (pair && !ext && pl.dz_bufs == 2) {
     // Merged backward: dZ of chunk 0 alone, then per chunk c one launch of
@@ -897,17 +990,18 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
         FLCE_CUDA(cudaMemsetAsync(mask_w, 0, mask_w_bytes, c.st));
       }
       const void* Wc = Wb16 + v0 * H;
+      const GemmParams p3 = dz_params(v0, w);
+      const Walk w3 = pick_walk(c.tun, pair, ext, p3);
       CUtensorMap tmWc_k, tmWc_mn, tmDzSt, tmDz_mn, tmDz_k, tmDw;
-      FLCE_TRY(map_kmajor(&tmWc_k, Wc, H, w, H, b_box_rows(pair)));
+      FLCE_TRY(map_kmajor(&tmWc_k, Wc, H, w, H, b_box_rows(pair, w3)));
       FLCE_TRY(map_mnmajor(&tmWc_mn, Wc, H, w, H));
       FLCE_TRY(map_dz_store(&tmDzSt, dz, w, N, Cv));
       FLCE_TRY(map_mnmajor(&tmDz_mn, dz, w, N, Cv));
-      FLCE_TRY(map_kmajor(&tmDz_k, dz, w, N, Cv, BM));
       FLCE_TRY(map_f32_out(&tmDw, dW + v0 * H, H, w, H));
 
       // K3: recompute Z[:, v0:v0+w] and write dZ (bf16) into the chunk scratch.
-      const GemmParams p3 = dz_params(v0, w);
-      FLCE_TRY((launch_tile<Epi::kDz, false, false>(pair, ext, dev, sms, tmX_k, tmWc_k, tmDzSt,
+      FLCE_TRY((launch_tile<Epi::kDz, false, false>(pair, ext, w3, dev, sms,
+                                                    w3.quad ? tmX_k64 : tmX_k, tmWc_k, tmDzSt,
                                                     p3, c.st, 1)));
 
       // K4: dW[v0:v0+w, :] = dZ_chunk^T X   (K = N tokens)
@@ -935,8 +1029,9 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
       p4.l2_keep_frac = l2_keep_fraction(c.tun, (double)N * H * 2);
       p4.err_word = c.err_word;
       p4.timeout_ns = kTimeoutNs;
-      FLCE_TRY((launch_tile<Epi::kStore, true, true>(pair, ext, dev, sms, tmDz_mn, tmX_mn, tmDw, p4,
-                                                     c.st, 2)));
+      FLCE_TRY((launch_tile<Epi::kStore, true, true>(pair, ext, pick_walk(c.tun, pair, ext, p4),
+                                                     dev, sms, tmDz_mn, tmX_mn, tmDw, p4, c.st,
+                                                     2)));
 
       // K5: dX_acc (+)= dZ_chunk W[v0:v0+w, :]   (K = w vocabulary columns)
       GemmParams p5{};
@@ -962,8 +1057,10 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
       p5.l2_keep_frac = l2_keep_fraction(c.tun, (double)w * H * 2);
       p5.err_word = c.err_word;
       p5.timeout_ns = kTimeoutNs;
-      FLCE_TRY((launch_tile<Epi::kStore, false, true>(pair, ext, dev, sms, tmDz_k, tmWc_mn, tmDxAcc,
-                                                      p5, c.st, 3)));
+      const Walk w5 = pick_walk(c.tun, pair, ext, p5);
+      FLCE_TRY(map_kmajor(&tmDz_k, dz, w, N, Cv, a_box_rows(w5)));
+      FLCE_TRY((launch_tile<Epi::kStore, false, true>(pair, ext, w5, dev, sms, tmDz_k, tmWc_mn,
+                                                      tmDxAcc, p5, c.st, 3)));
     }
   }
   if (c.dtype == FLCE_BF16 && !c.dx_partial_f32) {
@@ -1003,6 +1100,8 @@ const char* flce_status_string(flce_status s) {
 const char* flce_last_cuda_error(void) { return g_last_cuda_error.c_str(); }
 
 int flce_last_launch_count(void) { return g_launches; }
+
+int flce_debug_last_multicast_launches(void) { return g_quad_launches; }
 
 flce_status flce_profile_enable(int on) {
   g_prof_on = on != 0;
@@ -1050,6 +1149,13 @@ flce_status flce_set_cta_pair(int on) {
 
 int flce_cta_pair(void) { return g_cta_pair.load(); }
 
+flce_status flce_set_cluster_multicast(int on) {
+  g_cluster_mcast.store(on != 0 ? 1 : 0);
+  return FLCE_OK;
+}
+
+int flce_cluster_multicast(void) { return g_cluster_mcast.load(); }
+
 flce_status flce_set_backward_merge(int on) {
   if (on < 0 || on > 2) return FLCE_ERR_ARG;
   g_bwd_merge.store(on);
@@ -1089,6 +1195,7 @@ void flce_options_init(flce_options* opt) {
   opt->backward_merge = -1;
   opt->l2_hints = -1;
   opt->vocab_chunk = -1;
+  opt->cluster_multicast = -1;
 }
 
 }  // extern "C"
@@ -1104,7 +1211,7 @@ bool options_ok(const flce_options* opt) {
   if (opt->struct_size != sizeof(flce_options)) return false;
   auto tri = [](int v) { return v >= -1 && v <= 1; };
   return tri(opt->cta_pair) && opt->backward_merge >= -1 && opt->backward_merge <= 2 &&
-         tri(opt->l2_hints) &&
+         tri(opt->l2_hints) && tri(opt->cluster_multicast) &&
          opt->vocab_chunk >= -1;
 }
 
@@ -1117,6 +1224,7 @@ Tuning resolve_tuning(const flce_options* opt) {
   if (opt->backward_merge >= 0) t.merge = opt->backward_merge;
   if (opt->l2_hints >= 0) t.l2_hints = opt->l2_hints != 0;
   if (opt->vocab_chunk >= 0) t.chunk_set = opt->vocab_chunk;
+  if (opt->cluster_multicast >= 0) t.mcast = opt->cluster_multicast != 0;
   return t;
 }
 
@@ -1179,6 +1287,7 @@ flce_status flce_forward_ex(const void* X, const void* W, const int64_t* labels,
                             float* loss, float* lse, int32_t* valid_count, void* workspace,
                             size_t ws_bytes, int32_t* err_word, void* stream) {
   g_launches = 0;
+  g_quad_launches = 0;
   if (!options_ok(opt)) return FLCE_ERR_ARG;
   Common c = make_common(X, W, labels, N, H, V, dtype, opt, workspace, ws_bytes, err_word, stream);
   Plan pl;
@@ -1197,6 +1306,7 @@ flce_status flce_backward_ex(const void* X, const void* W, const int64_t* labels
                              const float* grad_loss, void* dX, float* dW, int accumulate_dW,
                              void* workspace, size_t ws_bytes, int32_t* err_word, void* stream) {
   g_launches = 0;
+  g_quad_launches = 0;
   if (!options_ok(opt)) return FLCE_ERR_ARG;
   Common c = make_common(X, W, labels, N, H, V, dtype, opt, workspace, ws_bytes, err_word, stream);
   Plan pl;
@@ -1217,6 +1327,7 @@ flce_status flce_fwd_bwd_ex(const void* X, const void* W, const int64_t* labels,
                             int32_t* valid_count, void* dX, float* dW, int accumulate_dW,
                             void* workspace, size_t ws_bytes, int32_t* err_word, void* stream) {
   g_launches = 0;
+  g_quad_launches = 0;
   if (!options_ok(opt)) return FLCE_ERR_ARG;
   Common c = make_common(X, W, labels, N, H, V, dtype, opt, workspace, ws_bytes, err_word, stream);
   Plan pl;
@@ -1297,6 +1408,7 @@ flce_status flce_forward_vocab_shard(const void* X, const void* W_shard, const i
                                      const flce_options* opt, float* partials, void* workspace,
                                      size_t ws_bytes, int32_t* err_word, void* stream) {
   g_launches = 0;
+  g_quad_launches = 0;
   Common c;
   FLCE_TRY(shard_common(X, W_shard, labels, N, H, V_shard, vocab_offset, vocab_total, dtype, opt,
                         workspace, ws_bytes, err_word, stream, &c));
@@ -1324,6 +1436,7 @@ flce_status flce_combine_vocab_shards(const float* partials, int n_shards, int64
                                       int32_t* valid_count, void* workspace, size_t ws_bytes,
                                       int32_t* err_word, void* stream) {
   g_launches = 0;
+  g_quad_launches = 0;
   if (!options_ok(opt) || opt->skip_ignored_blocks) return FLCE_ERR_ARG;
   if (n_shards <= 0 || N < 0 || N > (int64_t)INT32_MAX - 1024 || vocab_total <= 0 ||
       vocab_total > (int64_t)INT32_MAX - 1024)
@@ -1369,6 +1482,7 @@ flce_status flce_backward_vocab_shard(const void* X, const void* W_shard, const 
                                       float* dW_shard, int accumulate_dW, void* workspace,
                                       size_t ws_bytes, int32_t* err_word, void* stream) {
   g_launches = 0;
+  g_quad_launches = 0;
   Common c;
   FLCE_TRY(shard_common(X, W_shard, labels, N, H, V_shard, vocab_offset, vocab_total, dtype, opt,
                         workspace, ws_bytes, err_word, stream, &c));
@@ -1388,6 +1502,7 @@ flce_status flce_backward_vocab_shard(const void* X, const void* W_shard, const 
 flce_status flce_debug_wait_timeout(int32_t* err_word, uint64_t timeout_ns,
                                     int32_t* waited_us, void* stream) {
   g_launches = 0;
+  g_quad_launches = 0;
   if (!err_word || !waited_us || timeout_ns == 0 || timeout_ns > 10000000000ull)
     return FLCE_ERR_ARG;
   int dev, sms;
@@ -1403,6 +1518,7 @@ flce_status flce_debug_gemm(const void* A, const void* B, float* D, int64_t M, i
                             int64_t K, int a_mn, int b_mn, int accumulate, int32_t* err_word,
                             void* stream) {
   g_launches = 0;
+  g_quad_launches = 0;
   if (!A || !B || !D || !err_word) return FLCE_ERR_ARG;
   if (M <= 0 || Nn <= 0 || K <= 0 || M > INT32_MAX / 2 || Nn > INT32_MAX / 2 ||
       K > INT32_MAX / 2)
@@ -1413,13 +1529,8 @@ flce_status flce_debug_gemm(const void* A, const void* B, float* D, int64_t M, i
   int dev, sms;
   FLCE_TRY(device_check(&dev, &sms));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  CUtensorMap ta, tb, td;
-  if (a_mn) FLCE_TRY(map_mnmajor(&ta, A, M, K, M));
-  else FLCE_TRY(map_kmajor(&ta, A, K, M, K, BM));
-  const bool pair = g_cta_pair.load() != 0;
-  if (b_mn) FLCE_TRY(map_mnmajor(&tb, B, Nn, K, Nn));
-  else FLCE_TRY(map_kmajor(&tb, B, K, Nn, K, b_box_rows(pair)));
-  FLCE_TRY(map_f32_out(&td, D, Nn, M, Nn));
+  const Tuning tun = default_tuning();
+  const bool pair = tun.pair;
   GemmParams p{};
   p.m_size = (int)M;
   p.n_size = (int)Nn;
@@ -1433,10 +1544,17 @@ flce_status flce_debug_gemm(const void* A, const void* B, float* D, int64_t M, i
   p.reduce_add = accumulate ? 1 : 0;
   p.err_word = err_word;
   p.timeout_ns = kTimeoutNs;
-  if (!a_mn && !b_mn) return launch_tile<Epi::kStore, false, false>(pair, false, dev, sms, ta, tb, td, p, st);
-  if (!a_mn && b_mn) return launch_tile<Epi::kStore, false, true>(pair, false, dev, sms, ta, tb, td, p, st);
-  if (a_mn && !b_mn) return launch_tile<Epi::kStore, true, false>(pair, false, dev, sms, ta, tb, td, p, st);
-  return launch_tile<Epi::kStore, true, true>(pair, false, dev, sms, ta, tb, td, p, st);
+  const Walk w = pick_walk(tun, pair, false, p);
+  CUtensorMap ta, tb, td;
+  if (a_mn) FLCE_TRY(map_mnmajor(&ta, A, M, K, M));
+  else FLCE_TRY(map_kmajor(&ta, A, K, M, K, a_box_rows(w)));
+  if (b_mn) FLCE_TRY(map_mnmajor(&tb, B, Nn, K, Nn));
+  else FLCE_TRY(map_kmajor(&tb, B, K, Nn, K, b_box_rows(pair, w)));
+  FLCE_TRY(map_f32_out(&td, D, Nn, M, Nn));
+  if (!a_mn && !b_mn) return launch_tile<Epi::kStore, false, false>(pair, false, w, dev, sms, ta, tb, td, p, st);
+  if (!a_mn && b_mn) return launch_tile<Epi::kStore, false, true>(pair, false, w, dev, sms, ta, tb, td, p, st);
+  if (a_mn && !b_mn) return launch_tile<Epi::kStore, true, false>(pair, false, w, dev, sms, ta, tb, td, p, st);
+  return launch_tile<Epi::kStore, true, true>(pair, false, w, dev, sms, ta, tb, td, p, st);
 }
 
 }  // extern "C"

@@ -20,6 +20,14 @@
 //                 32 KB per SM instead of 48 KB; the leader CTA (rank 0) issues
 //                 the MMAs, which read both CTAs' shared memory and write each
 //                 CTA's 128 accumulator rows into its own TMEM.
+//   QUAD (CL = 4) the pair tiles, launched with 4-CTA clusters preferred: the
+//                 two pairs of a 4-CTA cluster take two tiles that share one
+//                 operand (B when they differ in row block, A when they differ
+//                 in column block) and walk them in step, each CTA loading one
+//                 64-row half of its share of that operand and multicasting it
+//                 to its counterpart in the other pair (rank ^ 2).  Operand
+//                 traffic from L2 drops by a quarter.  CTAs the hardware places
+//                 in 2-CTA clusters run the same tiles without multicast.
 //
 // D = A * B^T with A: M x K and B: N x K as the MMA sees them.  Either operand
 // may be K-major (K contiguous in memory) or MN-major (M/N contiguous):
@@ -396,9 +404,88 @@ __device__ __forceinline__ void staged_store(uint32_t buf, uint8_t* staging, int
   }
 }
 
-template <Epi EPI, bool A_MN, bool B_MN, int STAGES, bool PAIR, bool EXT>
+// QUAD launches: unit u goes to pair (u mod #pairs) as for pairs, and units
+// 2v, 2v+1 -- taken by the two pairs of one 4-CTA group in the same round --
+// share an operand: with SHARE_B the same column group g and row blocks
+// 2m, 2m+1 (row-block pairs walked like row blocks, bands halved); otherwise
+// the same row block and column groups 2h, 2h+1 (group length 1).  The host
+// only launches QUAD when these pairings cover the grid exactly.
+template <bool SHARE_B>
+__device__ __forceinline__ void unit_coords_quad(const GemmParams& p, int u, int& mb, int& nb0,
+                                                 int& nb1, int& g) {
+  const int i = u & 1;
+  const int v = u >> 1;
+  if constexpr (SHARE_B) {
+    const int mh = p.m_blocks >> 1;
+    int mbh;
+    if (p.m_fastest) {
+      const int band_h = p.m_band >> 1;
+      if (band_h > 0 && band_h < mh) {
+        const int band_units = band_h * p.n_groups;
+        const int band = v / band_units;
+        const int ub = v - band * band_units;
+        const int m0 = band * band_h;
+        const int mn = min(band_h, mh - m0);
+        mbh = m0 + ub % mn;
+        g = ub / mn;
+      } else {
+        mbh = v % mh;
+        g = v / mh;
+      }
+    } else {
+      g = v % p.n_groups;
+      mbh = v / p.n_groups;
+    }
+    mb = 2 * mbh + i;
+  } else {
+    const int gh = p.n_groups >> 1;
+    g = 2 * (v % gh) + i;
+    mb = v / gh;
+  }
+  nb0 = g * p.group_len;
+  nb1 = min(nb0 + p.group_len, p.n_blocks);
+  if (!dbg_ok(mb >= 0 && mb < p.m_blocks && g >= 0 && g < p.n_groups && nb0 < p.n_blocks,
+              p.err_word)) {
+    mb = 0;
+    g = 0;
+    nb0 = nb1 = 0;
+  }
+}
+
+// One CTA's 128-row half of an operand for one k-block, as two 64-row boxes
+// (8 KB each): K-major boxes are 64 rows x 64 k, MN-major boxes 64 MN x 64 k.
+// With `shared` and multicast the CTA loads only box `pic` and multicasts it
+// to itself and its counterpart in the other pair; otherwise both boxes.
+template <bool MN>
+__device__ __forceinline__ void load_half_quad(uint8_t* dst, const CUtensorMap* map, uint32_t bar,
+                                               int row0, int kb, bool shared, bool mcast,
+                                               uint32_t pic, uint16_t mask) {
+  if (shared && mcast) {
+    const int r = row0 + (int)pic * 64;
+    uint8_t* d = dst + pic * MN_BOX_BYTES;
+    if constexpr (MN)
+      tma_load_2d_pair_mcast(d, map, bar, r, kb * BK, mask);
+    else
+      tma_load_2d_pair_mcast(d, map, bar, kb * BK, r, mask);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      if constexpr (MN)
+        tma_load_2d_pair(dst + i * MN_BOX_BYTES, map, bar, row0 + i * 64, kb * BK);
+      else
+        tma_load_2d_pair(dst + i * MN_BOX_BYTES, map, bar, kb * BK, row0 + i * 64);
+    }
+  }
+}
+
+// CL: 1 single-CTA tiles, 2 CTA pairs, 4 CTA pairs with 4-CTA clusters
+// preferred (QUAD; EXT must be false).
+template <Epi EPI, bool A_MN, bool B_MN, int STAGES, int CL, bool EXT, bool SHARE_B = false>
 __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensorMap& tmB,
                                           const CUtensorMap& tmOut, const GemmParams& p) {
+  constexpr bool PAIR = CL >= 2;
+  constexpr bool QUAD = CL == 4;
+  static_assert(!(QUAD && EXT), "4-CTA clusters run only the plain kernels");
   using Cfg = TileCfg<PAIR>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -418,14 +505,22 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;  // 0 = leader (issues the MMAs)
+  const uint32_t crank = PAIR ? cluster_ctarank() : 0u;  // rank in the cluster
+  const uint32_t rank = crank & 1u;   // rank in the pair: 0 = leader (issues the MMAs)
+  const uint32_t lrank = crank & ~1u;  // cluster rank of this pair's leader
+  // QUAD: multicast only inside a 4-CTA cluster; pic = this pair's place in it
+  const bool mcast = QUAD && cluster_nctarank() == 4u;
+  const uint32_t pic = mcast ? (crank >> 1) : 0u;
+  const uint16_t mc_mask = (uint16_t)((1u << crank) | (1u << (crank ^ 2u)));
+  const uint16_t pair_mask = (uint16_t)(0x3u << lrank);
   const int pair_id = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
   const int num_pairs = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      // with multicast both pairs' MMAs read into this CTA's stages
+      mbar_init(&empty[s], mcast ? 2 : 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
@@ -476,7 +571,10 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
       }
       for (int u = pair_id; u < us.num_units && ok; u += num_pairs) {
         int mb, nb0, nb1, g;
-        unit_coords<EXT>(p, us, u, mb, nb0, nb1, g);
+        if constexpr (QUAD)
+          unit_coords_quad<SHARE_B>(p, u, mb, nb0, nb1, g);
+        else
+          unit_coords<EXT>(p, us, u, mb, nb0, nb1, g);
         const int a_row = mb * Cfg::TILE_M + (int)rank * BM;
         for (int nb = nb0; nb < nb1 && ok; ++nb) {
           const int b_row = nb * BN + (int)rank * Cfg::B_ROWS;
@@ -503,10 +601,17 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
             }
             uint8_t* a_dst = stages + s * Cfg::STAGE;
             uint8_t* b_dst = a_dst + Cfg::A_STAGE;
-            if constexpr (PAIR) {
+            if constexpr (QUAD) {
+              // The pair's bytes -- its own loads and the pieces the other
+              // pair multicasts into it -- complete on the leader's barrier.
+              const uint32_t bar = mapa_shared(smem_u32(&full[s]), lrank);
+              if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * Cfg::STAGE);
+              load_half_quad<A_MN>(a_dst, &tmA, bar, a_row, kb, !SHARE_B, mcast, pic, mc_mask);
+              load_half_quad<B_MN>(b_dst, &tmB, bar, b_row, kb, SHARE_B, mcast, pic, mc_mask);
+            } else if constexpr (PAIR) {
               // Both CTAs' loads complete on the leader's full barrier, which
               // only the leader arms with the pair's byte count.
-              const uint32_t bar = mapa_shared(smem_u32(&full[s]), 0);
+              const uint32_t bar = mapa_shared(smem_u32(&full[s]), lrank);
               if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * Cfg::STAGE);
               if constexpr (!EXT) {
                 if constexpr (!A_MN) {
@@ -609,7 +714,10 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
       bool ok = true;
       for (int u = pair_id; u < us.num_units && ok; u += num_pairs) {
         int mb, nb0, nb1, g;
-        unit_coords<EXT>(p, us, u, mb, nb0, nb1, g);
+        if constexpr (QUAD)
+          unit_coords_quad<SHARE_B>(p, u, mb, nb0, nb1, g);
+        else
+          unit_coords<EXT>(p, us, u, mb, nb0, nb1, g);
         for (int nb = nb0; nb < nb1 && ok; ++nb) {
           const uint32_t acc = tile & 1u;
           const uint32_t ra = tile >> 1;
@@ -644,7 +752,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
                 mma_issue(d_tmem, ad, bd, idesc, (ki | kk) != 0 ? 1u : 0u);
             }
             if constexpr (PAIR)
-              mma_commit_pair_multicast(&empty[s], 0x3);
+              mma_commit_pair_multicast(&empty[s], mcast ? (uint16_t)0xF : pair_mask);
             else
               mma_commit(&empty[s]);
             ++it;
@@ -652,7 +760,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
           }
           if (!ok) break;
           if constexpr (PAIR)
-            mma_commit_pair_multicast(&tfull[acc], 0x3);
+            mma_commit_pair_multicast(&tfull[acc], pair_mask);
           else
             mma_commit(&tfull[acc]);
           ++tile;
@@ -660,7 +768,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
       }
       // Every MMA this thread issued must finish before TMEM is released.
       if constexpr (PAIR)
-        mma_commit_pair_multicast(mma_done, 0x1);
+        mma_commit_pair_multicast(mma_done, (uint16_t)(1u << lrank));
       else
         mma_commit(mma_done);
       mbar_wait_drain(mma_done, 0, p.timeout_ns);
@@ -679,7 +787,10 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
 
     for (int u = pair_id; u < us.num_units && ok; u += num_pairs) {
       int mb, nb0, nb1, g;
-      unit_coords<EXT>(p, us, u, mb, nb0, nb1, g);
+      if constexpr (QUAD)
+        unit_coords_quad<SHARE_B>(p, u, mb, nb0, nb1, g);
+      else
+        unit_coords<EXT>(p, us, u, mb, nb0, nb1, g);
       const int row = mb * Cfg::TILE_M + row_in_tile;
       const int store_row0 = mb * Cfg::TILE_M + (int)rank * BM + q * 32;
       const bool row_ok = row < p.m_size;
@@ -809,7 +920,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
         __syncwarp();
         if (lane == 0) {
           if constexpr (PAIR)
-            mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
+            mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), lrank));
           else
             mbar_arrive(&tempty[acc]);
         }
@@ -854,7 +965,7 @@ template <Epi EPI, bool A_MN, bool B_MN, int STAGES, bool EXT = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmOut, const GemmParams p) {
-  gemm_body<EPI, A_MN, B_MN, STAGES, false, EXT>(tmA, tmB, tmOut, p);
+  gemm_body<EPI, A_MN, B_MN, STAGES, 1, EXT>(tmA, tmB, tmOut, p);
 }
 
 template <Epi EPI, bool A_MN, bool B_MN, int STAGES, bool EXT = false>
@@ -862,7 +973,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmOut, const GemmParams p) {
-  gemm_body<EPI, A_MN, B_MN, STAGES, true, EXT>(tmA, tmB, tmOut, p);
+  gemm_body<EPI, A_MN, B_MN, STAGES, 2, EXT>(tmA, tmB, tmOut, p);
+}
+
+// CTA pairs without compile-time cluster dimensions: launched with 2-CTA
+// clusters required and 4-CTA clusters preferred (QUAD above).
+template <Epi EPI, bool A_MN, bool B_MN, int STAGES, bool SHARE_B>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_quad_kernel(const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmOut, const GemmParams p) {
+  gemm_body<EPI, A_MN, B_MN, STAGES, 4, false, SHARE_B>(tmA, tmB, tmOut, p);
 }
 
 }  // namespace flce

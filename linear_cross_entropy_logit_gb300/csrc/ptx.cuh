@@ -350,6 +350,13 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
   return r;
 }
 
+// Number of CTAs in this CTA's cluster.
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t n;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
+  return n;
+}
+
 // Address of the same shared-memory location in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   uint32_t r;
@@ -383,6 +390,22 @@ __device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorM
       " [%0], [%1, {%3, %4}], [%2];"
       ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster_addr),
         "r"(x), "r"(y)
+      : "memory");
+}
+
+// tma_load_2d_pair multicast: the box lands at the same CTA-relative offset
+// in every CTA of `mask`, and each destination's bytes are signalled on the
+// mbarrier at the same offset in the even (MMA-issuing) CTA of that
+// destination's pair; `bar_cluster_addr` names that barrier in the issuing
+// CTA's own pair.
+__device__ __forceinline__ void tma_load_2d_pair_mcast(void* smem_dst, const CUtensorMap* map,
+                                                       uint32_t bar_cluster_addr, int32_t x,
+                                                       int32_t y, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;"
+      ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster_addr),
+        "r"(x), "r"(y), "h"(mask)
       : "memory");
 }
 

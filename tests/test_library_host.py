@@ -190,7 +190,8 @@ def test_options_struct_layout(L):
     assert o.struct_size == ctypes.sizeof(B.FlceOptions)
     assert (o.ignore_index, o.smoothing, o.z_loss, o.reduction, o.row_loss) == (-100, 0.0, 0.0, 0, None)
     assert (o.skip_ignored_blocks, o.grad_filter) == (0, 0.0)
-    assert (o.cta_pair, o.backward_merge, o.l2_hints, o.vocab_chunk) == (-1, -1, -1, -1)
+    assert (o.cta_pair, o.backward_merge, o.l2_hints, o.vocab_chunk,
+            o.cluster_multicast) == (-1, -1, -1, -1, -1)
     # a struct of another size is rejected before any CUDA call
     o.struct_size = 8
     P = ctypes.c_void_p
@@ -270,7 +271,7 @@ def test_options_launch_settings_size_the_workspace(L):
     assert B.flce_workspace_size(N, H, V, B.FLCE_BF16, B.MODE_BWD, old) == base
     # out-of-range settings are rejected (size 0)
     for field, bad in (("cta_pair", 2), ("backward_merge", -2), ("l2_hints", 3),
-                       ("vocab_chunk", -5)):
+                       ("vocab_chunk", -5), ("cluster_multicast", 2)):
         o = B.make_options()
         setattr(o, field, bad)
         assert B.flce_workspace_size(N, H, V, B.FLCE_BF16, B.MODE_BWD, o) == 0, field
