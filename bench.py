@@ -120,7 +120,7 @@ def summarize_traffic(csv_path: str, workload: str, shape=None) -> None:
     for r in rows:
         name = r["Kernel Name"]
         m = (re.search(r"EpiE(\d)ELb(\d)ELb(\d)", name)
-             or re.search(r"gemm_(?:pair_)?kernel<(\d), (\d), (\d), \d+(?:, \d)?>", name))
+             or re.search(r"gemm_(?:pair_|quad_)?kernel<(\d), (\d), (\d), \d+(?:, \d)?>", name))
         if "bwd_fused_kernel" in name:
             kind = "bwd_merged"
         elif m:
@@ -411,6 +411,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     base_mem = torch.cuda.memory_allocated(dev)  # inputs and outputs only
     ws = B.workspace(N, H, V, dt, B.MODE_FWD_BWD, dev)
 
+    mc_launches = [0]  # GEMM launches that took the operand-multicast walk
     if args.vocab_shards > 1:
         P = args.vocab_shards
         bounds = [round(V * i / P / 256) * 256 for i in range(P)] + [V]
@@ -443,6 +444,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                            lse=lse, valid_count=nv, dX=dX, dW=dW, workspace_buf=ws, err_word=err,
                            stream=stream, z_loss=args.z_loss,
                            skip_ignored_blocks=args.skip_ignored, grad_filter=args.grad_filter)
+            mc_launches[0] += B.last_multicast_launches()
             return B.last_launch_count()
     if args.vocab_shards > 1:
         args.no_e2e = True  # the end-to-end leg times the unsharded call only
@@ -466,8 +468,10 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     wall0 = time.perf_counter()
     ev0.record(stream)
     launches = 0
+    mc_launches[0] = 0
     for _ in range(args.steps):
         launches += step()
+    launches_mc = mc_launches[0]
     ev1.record(stream)
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - wall0
@@ -695,6 +699,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "e2e": e2e,
         "e2e_all_outputs": e2e_all,
         "gpu_launches": launches,
+        "gpu_launches_multicast": launches_mc,
         "clocks": clocks,
         "wall_s_timed": wall,
         "memory": extra,
