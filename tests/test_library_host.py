@@ -280,7 +280,7 @@ def test_options_launch_settings_size_the_workspace(L):
     assert B.flce_workspace_size(N, H, V, B.FLCE_BF16, B.MODE_BWD, old) == base
     # out-of-range settings are rejected (size 0)
     for field, bad in (("cta_pair", 2), ("backward_merge", -2), ("l2_hints", 3),
-                       ("vocab_chunk", -5), ("cluster_multicast", 3)):
+                       ("vocab_chunk", -5), ("cluster_multicast", 2)):
         o = B.make_options()
         setattr(o, field, bad)
         assert B.flce_workspace_size(N, H, V, B.FLCE_BF16, B.MODE_BWD, o) == 0, field
