@@ -68,9 +68,9 @@ def parse_args():
                     help="skip token blocks whose labels are all ignore_index")
     ap.add_argument("--z-loss", type=float, default=0.0,
                     help="z-loss weight alpha (adds alpha * lse^2 per valid token)")
-    ap.add_argument("--multicast", type=int, default=None, choices=(0, 1, 2),
-                    help="operand multicast between CTA pairs: groups of up to four pairs (1), "
-                         "of two pairs (2), or plain CTA pairs (0); default: the library's")
+    ap.add_argument("--multicast", type=int, default=None, choices=(0, 1),
+                    help="operand multicast between CTA pairs in 4-CTA clusters (1) or plain "
+                         "CTA pairs (0); default: the library's default")
     ap.add_argument("--single-cta", action="store_true",
                     help="128x256 single-CTA tiles instead of 256x256 CTA-pair tiles")
     ap.add_argument("--clocks-dir", default=None,
@@ -384,7 +384,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     B.flce_set_l2_hints(args.l2_hints)
     B.flce_set_cta_pair(not args.single_cta)
     if args.multicast is not None:
-        B.flce_set_cluster_multicast(args.multicast)
+        B.flce_set_cluster_multicast(bool(args.multicast))
     if args.merge is not None:
         B.flce_set_backward_merge(args.merge)
     merge_mode = B.flce_backward_merge()
@@ -411,7 +411,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     base_mem = torch.cuda.memory_allocated(dev)  # inputs and outputs only
     ws = B.workspace(N, H, V, dt, B.MODE_FWD_BWD, dev)
 
-    mc_launches = [0, 0]  # GEMM launches with the operand-multicast walk: all, groups of 4
+    mc_launches = [0]  # GEMM launches that took the operand-multicast walk
     if args.vocab_shards > 1:
         P = args.vocab_shards
         bounds = [round(V * i / P / 256) * 256 for i in range(P)] + [V]
@@ -444,8 +444,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                            lse=lse, valid_count=nv, dX=dX, dW=dW, workspace_buf=ws, err_word=err,
                            stream=stream, z_loss=args.z_loss,
                            skip_ignored_blocks=args.skip_ignored, grad_filter=args.grad_filter)
-            mc_launches[0] += B.last_multicast_launches(0)
-            mc_launches[1] += B.last_multicast_launches(4)
+            mc_launches[0] += B.last_multicast_launches()
             return B.last_launch_count()
     if args.vocab_shards > 1:
         args.no_e2e = True  # the end-to-end leg times the unsharded call only
@@ -469,10 +468,10 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     wall0 = time.perf_counter()
     ev0.record(stream)
     launches = 0
-    mc_launches[0] = mc_launches[1] = 0
+    mc_launches[0] = 0
     for _ in range(args.steps):
         launches += step()
-    launches_mc = list(mc_launches)
+    launches_mc = mc_launches[0]
     ev1.record(stream)
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - wall0
@@ -700,7 +699,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "e2e": e2e,
         "e2e_all_outputs": e2e_all,
         "gpu_launches": launches,
-        "gpu_launches_multicast": {"all": launches_mc[0], "groups_of_4_pairs": launches_mc[1]},
+        "gpu_launches_multicast": launches_mc,
         "clocks": clocks,
         "wall_s_timed": wall,
         "memory": extra,

@@ -114,21 +114,17 @@ flce_status flce_set_cta_pair(int on);
 int flce_cta_pair(void);
 
 /* Operand multicast between CTA pairs, process-wide default (options field
- * cluster_multicast overrides it per call).  A CTA-pair GEMM launch of the
- * plain kernels (none of skip_ignored_blocks, grad_filter, L2 hints) whose
- * tiles group exactly -- row blocks in groups sharing each column block, or
- * column blocks in groups sharing each row block -- walks them in groups of
- * G pairs that compute G such tiles in step and multicast the operand they
- * share (TMA .multicast), each CTA loading 1/G of its share of it:
- *   1 (the default): G = 4 where the counts divide by four (8-CTA clusters
- *     preferred, 4-CTA clusters where the hardware cannot place eight, those
- *     sharing between two pairs), else G = 2 (4-CTA clusters preferred,
- *     2-CTA clusters without multicast where it cannot place four);
- *   2: G = 2 only;
- *   0: plain CTA pairs.
- * Results are bit-identical in every mode.  Not used by the merged backward
- * launches.  Other values return FLCE_ERR_ARG. */
-flce_status flce_set_cluster_multicast(int mode);
+ * cluster_multicast overrides it per call).  1 (the default): a CTA-pair GEMM
+ * launch of the plain kernels (none of skip_ignored_blocks, grad_filter, L2
+ * hints) whose tiles pair up -- an even number of row blocks sharing each
+ * column block, or of column blocks sharing each row block -- is launched
+ * with 4-CTA clusters preferred; the two pairs of a 4-CTA cluster compute two
+ * such tiles in step and multicast the operand they share (TMA .multicast),
+ * so each loads a quarter less from L2.  The hardware may group any four CTAs
+ * as two 2-CTA clusters instead; those compute the same tiles without
+ * multicast.  0: plain CTA pairs.  Results are bit-identical either way.
+ * Not used by the merged backward launches. */
+flce_status flce_set_cluster_multicast(int on);
 int flce_cluster_multicast(void);
 
 /* Backward layout, process-wide default (options field backward_merge
@@ -234,7 +230,7 @@ flce_status flce_fwd_bwd(const void* X, const void* W, const int64_t* labels, in
  *   l2_hints        -1, 0 or 1: see flce_set_l2_hints
  *   vocab_chunk     -1, 0 (automatic width) or a width in columns: see
  *                   flce_set_vocab_chunk
- *   cluster_multicast -1, 0, 1 or 2: see flce_set_cluster_multicast
+ *   cluster_multicast -1, 0 or 1: see flce_set_cluster_multicast
  * The workspace of a call must be sized with the same settings:
  * flce_workspace_size_ex with the same options.  A struct from a caller built
  * against ABI 1.05 (struct_size = offsetof(flce_options, cta_pair)) is
@@ -383,10 +379,10 @@ int flce_abi_version(void);
 flce_status flce_debug_wait_timeout(int32_t* err_word, uint64_t timeout_ns, int32_t* waited_us,
                                     void* stream);
 
-/* TEST-ONLY: how many GEMM launches of the last call on this thread took the
- * operand-multicast walk of flce_set_cluster_multicast with groups of
- * pairs_per_group pairs (2 or 4; any other value: both). */
-int flce_debug_last_multicast_launches(int pairs_per_group);
+/* TEST-ONLY: how many GEMM launches of the last call on this thread were made
+ * with 4-CTA clusters preferred (the operand-multicast walk of
+ * flce_set_cluster_multicast). */
+int flce_debug_last_multicast_launches(void);
 
 /* TEST-ONLY: the library's tcgen05 GEMM core without a loss epilogue.
  * D (M x Nn fp32, device, row-major) = A * B^T, or += when accumulate != 0,

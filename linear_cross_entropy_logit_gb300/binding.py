@@ -174,7 +174,7 @@ def load(path: str) -> ctypes.CDLL:
     L.flce_set_cluster_multicast.restype = I32
     L.flce_cluster_multicast.argtypes = []
     L.flce_cluster_multicast.restype = I32
-    L.flce_debug_last_multicast_launches.argtypes = [I32]
+    L.flce_debug_last_multicast_launches.argtypes = []
     L.flce_debug_last_multicast_launches.restype = I32
     return L
 
@@ -251,15 +251,14 @@ def flce_cta_pair() -> bool:
     return bool(lib().flce_cta_pair())
 
 
-def flce_set_cluster_multicast(mode) -> None:
-    """Operand multicast between CTA pairs: 1 (or True) groups of up to four
-    pairs (default), 2 groups of two pairs, 0 (or False) plain CTA pairs.
-    Bit-identical results in every mode."""
-    _check(lib().flce_set_cluster_multicast(int(mode)), "flce_set_cluster_multicast")
+def flce_set_cluster_multicast(on: bool) -> None:
+    """1: pair launches whose tiles pair up take 4-CTA clusters with operand
+    multicast (default); 0: plain CTA pairs.  Bit-identical results."""
+    _check(lib().flce_set_cluster_multicast(int(bool(on))), "flce_set_cluster_multicast")
 
 
-def flce_cluster_multicast() -> int:
-    return int(lib().flce_cluster_multicast())
+def flce_cluster_multicast() -> bool:
+    return bool(lib().flce_cluster_multicast())
 
 
 def flce_set_backward_merge(mode) -> None:
@@ -297,7 +296,7 @@ def make_options(ignore_index: int = -100, smoothing: float = 0.0, reduction: st
                  grad_filter: float = 0.0, *, cta_pair: Optional[bool] = None,
                  backward_merge: Optional[int] = None, l2_hints: Optional[bool] = None,
                  vocab_chunk: Optional[int] = None,
-                 cluster_multicast: Optional[int] = None) -> FlceOptions:
+                 cluster_multicast: Optional[bool] = None) -> FlceOptions:
     """An ``flce_options``; the launch settings left at None take the
     process-wide defaults at the time of each call."""
     o = FlceOptions()
@@ -318,7 +317,7 @@ def make_options(ignore_index: int = -100, smoothing: float = 0.0, reduction: st
     if vocab_chunk is not None:
         o.vocab_chunk = int(vocab_chunk)
     if cluster_multicast is not None:
-        o.cluster_multicast = int(cluster_multicast)
+        o.cluster_multicast = int(bool(cluster_multicast))
     return o
 
 
@@ -572,10 +571,9 @@ def last_launch_count() -> int:
     return int(lib().flce_last_launch_count())
 
 
-def last_multicast_launches(pairs_per_group: int = 0) -> int:
-    """Test-only: launches of the last call that took the operand-multicast walk
-    with groups of 2 or 4 pairs (0: either)."""
-    return int(lib().flce_debug_last_multicast_launches(pairs_per_group))
+def last_multicast_launches() -> int:
+    """Test-only: launches of the last call made with the operand-multicast walk."""
+    return int(lib().flce_debug_last_multicast_launches())
 
 
 def flce_profile_enable(on: bool) -> None:

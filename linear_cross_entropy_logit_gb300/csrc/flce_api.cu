@@ -51,14 +51,14 @@ constexpr size_t kAlign = 256;
 
 thread_local std::string g_last_cuda_error;
 thread_local int g_launches = 0;
-thread_local int g_quad_launches[2] = {0, 0};  // last call's multicast launches: groups of 2, 4 pairs
+thread_local int g_quad_launches = 0;  // launches of the last call that took the QUAD walk
 // Process-wide defaults of the launch settings; a call whose options set a
 // field itself does not read the matching default.
 std::atomic<int64_t> g_vocab_chunk{0};
 std::atomic<int> g_cta_pair{1};
 std::atomic<int> g_bwd_merge{0};
 std::atomic<int> g_l2_hints{0};
-std::atomic<int> g_cluster_mcast{1};  // 0 off, 1 groups of up to 4 pairs, 2 groups of 2 pairs
+std::atomic<int> g_cluster_mcast{1};
 
 // Launch settings of one call, resolved once at its entry from its options
 // and the process-wide defaults, and used for both the workspace plan and the
@@ -70,12 +70,12 @@ struct Tuning {
                        // 2 dW(c) + dX(c) merged after dZ(c) (one dZ buffer)
   bool l2_hints;       // evict_last policy on the re-read operand
   int64_t chunk_set;   // requested vocabulary chunk width (0 = automatic)
-  int mcast;           // operand multicast: 0 off, 1 groups of up to 4 pairs, 2 of 2 pairs
+  bool mcast;          // pair launches may take 4-CTA clusters with operand multicast
 };
 
 Tuning default_tuning() {
   return Tuning{g_cta_pair.load() != 0, g_bwd_merge.load(), g_l2_hints.load() != 0,
-                g_vocab_chunk.load(), g_cluster_mcast.load()};
+                g_vocab_chunk.load(), g_cluster_mcast.load() != 0};
 }
 
 // Optional per-kernel timing: CUDA events recorded on the caller's stream
@@ -378,8 +378,8 @@ flce_status map_kmajor(CUtensorMap* m, const void* base, uint64_t k, uint64_t ro
                   box_rows);
 }
 flce_status map_mnmajor(CUtensorMap* m, const void* base, uint64_t mn, uint64_t k,
-                        uint64_t pitch_elems, uint32_t box_k = BK) {
-  return make_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, mn, k, pitch_elems * 2, 64, box_k);
+                        uint64_t pitch_elems) {
+  return make_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, mn, k, pitch_elems * 2, 64, BK);
 }
 // dZ chunk store map: 64 bf16 columns x 32 rows
 flce_status map_dz_store(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
@@ -464,79 +464,47 @@ flce_status launch_gemm(int dev, int num_sms, const CUtensorMap& a, const CUtens
 // operand their tiles share; see gemm_core.cuh).
 struct Walk {
   bool quad = false;
-  bool share_b = false;  // QUAD: the pairs of a group share B (differ in row block), else A
-  int group = 2;         // QUAD: pairs per group (2: 4-CTA clusters, 4: 8-CTA clusters)
+  bool share_b = false;  // QUAD: the pairs share B (differ in row block), else A
 };
 
-// A multicast walk needs whole groups of G pairs whose units group exactly:
-// units G*v .. G*v + G-1 must differ only in the row block (share B) or only
-// in the column group (share A, group length 1), and every unit needs its
-// partners.  Groups of four pairs are taken where they fit (and the setting
-// allows), else groups of two.
-bool walk_fits(const GemmParams& p, int G, bool* share_b) {
-  if (p.num_units < 2 * G || p.num_units % G != 0) return false;
-  if (p.m_fastest) {
-    const bool banded = p.m_band > 0 && p.m_band < p.m_blocks;
-    if (p.m_blocks % G != 0 || (banded && p.m_band % G != 0)) return false;
-    *share_b = true;
-    return true;
-  }
-  if (p.group_len == 1 && p.n_groups % G == 0) {
-    *share_b = false;
-    return true;
-  }
-  if (p.m_blocks % G == 0) {
-    *share_b = true;
-    return true;
-  }
-  return false;
-}
-
+// QUAD needs whole groups of two pairs whose units pair up exactly: units
+// 2v and 2v+1 must differ only in the row block (share B) or only in the
+// column group (share A, group length 1), and every unit needs its partner.
 Walk pick_walk(const Tuning& t, bool pair, bool ext, const GemmParams& p) {
   Walk w;
-  if (!pair || ext || t.mcast == 0) return w;
-  for (int G : {4, 2}) {
-    if (G == 4 && t.mcast == 2) continue;
-    if (walk_fits(p, G, &w.share_b)) {
-      w.quad = true;
-      w.group = G;
-      return w;
-    }
+  if (!pair || ext || !t.mcast || p.num_units < 4 || p.num_units % 2 != 0) return w;
+  if (p.m_fastest) {
+    const bool banded = p.m_band > 0 && p.m_band < p.m_blocks;
+    if (p.m_blocks % 2 != 0 || (banded && p.m_band % 2 != 0)) return w;
+    w.quad = w.share_b = true;
+  } else if (p.group_len == 1 && p.n_groups % 2 == 0) {
+    w.quad = true;
+  } else if (p.m_blocks % 2 == 0) {
+    w.quad = w.share_b = true;
   }
   return w;
 }
 
-// Box of an operand map.  K-major: rows per box -- 128 for A and 128 (pairs)
-// or 256 (single CTAs) for B in the plain walks; 64 in the multicast walks,
-// 32 for the shared operand of a group of four pairs.  MN-major: k-rows per
-// 64-column box -- 64, or 16 for the shared operand of a group of four pairs.
-bool shared_operand(const Walk& w, bool is_a) { return w.quad && (is_a ? !w.share_b : w.share_b); }
-uint32_t kmajor_box(bool pair, const Walk& w, bool is_a) {
-  if (!w.quad) return is_a ? BM : (pair ? BN / 2 : BN);
-  return (shared_operand(w, is_a) && w.group == 4) ? 32 : 64;
-}
-uint32_t mnmajor_box_k(const Walk& w, bool is_a) {
-  return (shared_operand(w, is_a) && w.group == 4) ? 16 : BK;
-}
+// Rows of a K-major operand box: QUAD loads every operand half as two 64-row
+// boxes; pairs load their 128 rows of A and of B in one box each, single CTAs
+// 128 rows of A and 256 of B.
+uint32_t a_box_rows(const Walk& w) { return w.quad ? 64 : BM; }
+uint32_t b_box_rows(bool pair, const Walk& w) { return w.quad ? 64 : (pair ? BN / 2 : BN); }
 
-template <Epi EPI, bool A_MN, bool B_MN, bool SHARE_B, int GROUP>
+template <Epi EPI, bool A_MN, bool B_MN, bool SHARE_B>
 flce_status launch_quad(int dev, int num_sms, const CUtensorMap& a, const CUtensorMap& b,
                         const CUtensorMap& out, const GemmParams& p, cudaStream_t st,
                         int prof_kind) {
-  auto kern = gemm_quad_kernel<EPI, A_MN, B_MN, kPairStages, SHARE_B, GROUP>;
+  auto kern = gemm_quad_kernel<EPI, A_MN, B_MN, kPairStages, SHARE_B>;
   constexpr int smem = gemm_smem_bytes<EPI, kPairStages, true, false>();
   static KernelSetup setup[kMaxDevices];
   setup_kernel(setup[dev], kern, smem, false, num_sms);
   if (setup[dev].err != cudaSuccess) return cuda_fail(setup[dev].err, setup[dev].what);
   if (p.num_units <= 0) return FLCE_OK;
-  // A multiple of GROUP pairs, so that the pairs of every group of 2 * GROUP
-  // CTAs take partner units.  Groups of two pairs: 2-CTA clusters required,
-  // 4-CTA clusters preferred (the hardware makes a group of four CTAs one
-  // 4-CTA cluster where it can, else two 2-CTA clusters without multicast).
-  // Groups of four pairs: 4-CTA clusters required, 8-CTA clusters preferred
-  // (on a 152-SM GB300: 16 clusters of eight and 6 of four).
-  const int pairs = std::min(p.num_units, num_sms / 2) / GROUP * GROUP;
-  if (pairs <= 0) return FLCE_ERR_UNSUPPORTED;
+  // An even number of pairs, so that the two pairs of every group of four
+  // CTAs take partner units; the hardware groups each four into one 4-CTA
+  // cluster where it can, else into two 2-CTA clusters (no multicast).
+  const int pairs = std::min(p.num_units, num_sms / 2) & ~1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * pairs, 1, 1);
   cfg.blockDim = dim3(NUM_THREADS, 1, 1);
@@ -544,11 +512,11 @@ flce_status launch_quad(int dev, int num_sms, const CUtensorMap& a, const CUtens
   cfg.stream = st;
   cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = GROUP == 4 ? 4 : 2;
+  at[0].val.clusterDim.x = 2;
   at[0].val.clusterDim.y = 1;
   at[0].val.clusterDim.z = 1;
   at[1].id = cudaLaunchAttributePreferredClusterDimension;
-  at[1].val.preferredClusterDim.x = 2 * GROUP;
+  at[1].val.preferredClusterDim.x = 4;
   at[1].val.preferredClusterDim.y = 1;
   at[1].val.preferredClusterDim.z = 1;
   cfg.attrs = at;
@@ -561,7 +529,7 @@ flce_status launch_quad(int dev, int num_sms, const CUtensorMap& a, const CUtens
   }
   FLCE_CUDA(cudaLaunchKernelEx(&cfg, kern, a, b, out, p));
   ++g_launches;
-  ++g_quad_launches[GROUP == 4 ? 1 : 0];
+  ++g_quad_launches;
   if (rec.start && rec.stop) {
     FLCE_CUDA(cudaEventRecord(rec.stop, st));
     g_prof_pending.push_back(rec);
@@ -575,15 +543,9 @@ template <Epi EPI, bool A_MN, bool B_MN>
 flce_status launch_tile(bool pair, bool ext, const Walk& w, int dev, int num_sms,
                         const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out,
                         const GemmParams& p, cudaStream_t st, int prof_kind = -1) {
-  if (w.quad) {
-    if (w.group == 4)
-      return w.share_b
-                 ? launch_quad<EPI, A_MN, B_MN, true, 4>(dev, num_sms, a, b, out, p, st, prof_kind)
-                 : launch_quad<EPI, A_MN, B_MN, false, 4>(dev, num_sms, a, b, out, p, st, prof_kind);
-    return w.share_b
-               ? launch_quad<EPI, A_MN, B_MN, true, 2>(dev, num_sms, a, b, out, p, st, prof_kind)
-               : launch_quad<EPI, A_MN, B_MN, false, 2>(dev, num_sms, a, b, out, p, st, prof_kind);
-  }
+  if (w.quad)
+    return w.share_b ? launch_quad<EPI, A_MN, B_MN, true>(dev, num_sms, a, b, out, p, st, prof_kind)
+                     : launch_quad<EPI, A_MN, B_MN, false>(dev, num_sms, a, b, out, p, st, prof_kind);
   if (ext)
     return pair ? launch_gemm<EPI, A_MN, B_MN, true, true>(dev, num_sms, a, b, out, p, st, prof_kind)
                 : launch_gemm<EPI, A_MN, B_MN, false, true>(dev, num_sms, a, b, out, p, st, prof_kind);
@@ -629,15 +591,11 @@ flce_status launch_fused(int dev, int num_sms, const FusedMaps& maps, const Fuse
 // one more pass over W per band but keeps each band's X resident; measured on
 // a GB300 it cut the dZ launch's DRAM reads from ~1.0 to 0.42 GB at the
 // Llama-3 shape and sped the step up ~2% (Llama-3 and Gemma-2 shapes).
-// Band sizes are rounded up to a multiple of four row blocks, so that the
-// multicast walks' groups of two or four row blocks never straddle a band.
 int x_band(int64_t N, int64_t H, int m_blocks) {
   const double x_bytes = (double)N * H * 2;
   if (x_bytes <= 48.0 * (1 << 20)) return 0;
   const int bands = (int)std::min(4.0, std::ceil(x_bytes / (40.0 * (1 << 20))));
-  if (bands <= 1) return 0;
-  const int band = ((m_blocks + bands - 1) / bands + 3) / 4 * 4;
-  return band < m_blocks ? band : 0;
+  return bands > 1 ? (m_blocks + bands - 1) / bands : 0;
 }
 
 // Fraction of the reused operand's lines kept in L2 with evict_last priority:
@@ -805,8 +763,8 @@ flce_status run_forward(const Common& c, const Plan& pl, int dev, int sms, const
     const bool ext = ext_features(c);
     const Walk walk = pick_walk(c.tun, pair, ext, p);
     CUtensorMap tmX, tmW;
-    FLCE_TRY(map_kmajor(&tmX, Xb, c.H, c.N, c.H, kmajor_box(pair, walk, true)));
-    FLCE_TRY(map_kmajor(&tmW, Wb, c.H, c.V, c.H, kmajor_box(pair, walk, false)));
+    FLCE_TRY(map_kmajor(&tmX, Xb, c.H, c.N, c.H, a_box_rows(walk)));
+    FLCE_TRY(map_kmajor(&tmW, Wb, c.H, c.V, c.H, b_box_rows(pair, walk)));
     FLCE_TRY((launch_tile<Epi::kLse, false, false>(pair, ext, walk, dev, sms, tmX, tmW, tmX, p,
                                                   c.st, 0)));
     if (shard_out) {
@@ -853,11 +811,9 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
 
   // X as the K-major A operand of the dZ recompute: 128-row boxes (pairs, the
   // merged launches) or 64-row boxes (QUAD walks)
-  CUtensorMap tmX_k, tmX_k64, tmX_mn, tmX_mn16, tmDxAcc;
+  CUtensorMap tmX_k, tmX_k64, tmX_mn, tmDxAcc;
   FLCE_TRY(map_kmajor(&tmX_k, Xb, H, N, H, BM));
   FLCE_TRY(map_kmajor(&tmX_k64, Xb, H, N, H, 64));
-  // X as the MN-major B operand of dW when a group of four pairs shares it
-  FLCE_TRY(map_mnmajor(&tmX_mn16, Xb, H, N, H, 16));
   FLCE_TRY(map_mnmajor(&tmX_mn, Xb, H, N, H));
   FLCE_TRY(map_f32_out(&tmDxAcc, dx_acc, H, N, H));
 
@@ -1002,9 +958,8 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
     const int64_t w = std::min(Cv, V - v0);
     const GemmParams p3 = dz_params(v0, w);
     const Walk w3 = pick_walk(c.tun, pair, ext_kernel, p3);
-    if (shared_operand(w3, true)) return FLCE_ERR_UNSUPPORTED;  // the dZ walks share W only
     CUtensorMap tmWc_k, tmDzSt;
-    FLCE_TRY(map_kmajor(&tmWc_k, Wb16 + v0 * H, H, w, H, kmajor_box(pair, w3, false)));
+    FLCE_TRY(map_kmajor(&tmWc_k, Wb16 + v0 * H, H, w, H, b_box_rows(pair, w3)));
     FLCE_TRY(map_dz_store(&tmDzSt, buf, w, N, Cv));
     return launch_tile<Epi::kDz, false, false>(pair, ext_kernel, w3, dev, sms,
                                                w3.quad ? tmX_k64 : tmX_k, tmWc_k, tmDzSt, p3,
@@ -1037,10 +992,11 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
       const void* Wc = Wb16 + v0 * H;
       const GemmParams p3 = dz_params(v0, w);
       const Walk w3 = pick_walk(c.tun, pair, ext, p3);
-      if (shared_operand(w3, true)) return FLCE_ERR_UNSUPPORTED;  // the dZ walks share W only
       CUtensorMap tmWc_k, tmWc_mn, tmDzSt, tmDz_mn, tmDz_k, tmDw;
-      FLCE_TRY(map_kmajor(&tmWc_k, Wc, H, w, H, kmajor_box(pair, w3, false)));
+      FLCE_TRY(map_kmajor(&tmWc_k, Wc, H, w, H, b_box_rows(pair, w3)));
+      FLCE_TRY(map_mnmajor(&tmWc_mn, Wc, H, w, H));
       FLCE_TRY(map_dz_store(&tmDzSt, dz, w, N, Cv));
+      FLCE_TRY(map_mnmajor(&tmDz_mn, dz, w, N, Cv));
       FLCE_TRY(map_f32_out(&tmDw, dW + v0 * H, H, w, H));
 
       // K3: recompute Z[:, v0:v0+w] and write dZ (bf16) into the chunk scratch.
@@ -1073,12 +1029,9 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
       p4.l2_keep_frac = l2_keep_fraction(c.tun, (double)N * H * 2);
       p4.err_word = c.err_word;
       p4.timeout_ns = kTimeoutNs;
-      const Walk w4 = pick_walk(c.tun, pair, ext, p4);
-      FLCE_TRY(map_mnmajor(&tmDz_mn, dz, w, N, Cv, mnmajor_box_k(w4, true)));
-      FLCE_TRY((launch_tile<Epi::kStore, true, true>(pair, ext, w4, dev, sms, tmDz_mn,
-                                                     mnmajor_box_k(w4, false) == BK ? tmX_mn
-                                                                                    : tmX_mn16,
-                                                     tmDw, p4, c.st, 2)));
+      FLCE_TRY((launch_tile<Epi::kStore, true, true>(pair, ext, pick_walk(c.tun, pair, ext, p4),
+                                                     dev, sms, tmDz_mn, tmX_mn, tmDw, p4, c.st,
+                                                     2)));
 
       // K5: dX_acc (+)= dZ_chunk W[v0:v0+w, :]   (K = w vocabulary columns)
       GemmParams p5{};
@@ -1105,8 +1058,7 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
       p5.err_word = c.err_word;
       p5.timeout_ns = kTimeoutNs;
       const Walk w5 = pick_walk(c.tun, pair, ext, p5);
-      FLCE_TRY(map_kmajor(&tmDz_k, dz, w, N, Cv, kmajor_box(pair, w5, true)));
-      FLCE_TRY(map_mnmajor(&tmWc_mn, Wc, H, w, H, mnmajor_box_k(w5, false)));
+      FLCE_TRY(map_kmajor(&tmDz_k, dz, w, N, Cv, a_box_rows(w5)));
       FLCE_TRY((launch_tile<Epi::kStore, false, true>(pair, ext, w5, dev, sms, tmDz_k, tmWc_mn,
                                                       tmDxAcc, p5, c.st, 3)));
     }
@@ -1149,11 +1101,7 @@ const char* flce_last_cuda_error(void) { return g_last_cuda_error.c_str(); }
 
 int flce_last_launch_count(void) { return g_launches; }
 
-int flce_debug_last_multicast_launches(int pairs_per_group) {
-  if (pairs_per_group == 2) return g_quad_launches[0];
-  if (pairs_per_group == 4) return g_quad_launches[1];
-  return g_quad_launches[0] + g_quad_launches[1];
-}
+int flce_debug_last_multicast_launches(void) { return g_quad_launches; }
 
 flce_status flce_profile_enable(int on) {
   g_prof_on = on != 0;
@@ -1201,9 +1149,8 @@ flce_status flce_set_cta_pair(int on) {
 
 int flce_cta_pair(void) { return g_cta_pair.load(); }
 
-flce_status flce_set_cluster_multicast(int mode) {
-  if (mode < 0 || mode > 2) return FLCE_ERR_ARG;
-  g_cluster_mcast.store(mode);
+flce_status flce_set_cluster_multicast(int on) {
+  g_cluster_mcast.store(on != 0 ? 1 : 0);
   return FLCE_OK;
 }
 
@@ -1264,7 +1211,7 @@ bool options_ok(const flce_options* opt) {
   if (opt->struct_size != sizeof(flce_options)) return false;
   auto tri = [](int v) { return v >= -1 && v <= 1; };
   return tri(opt->cta_pair) && opt->backward_merge >= -1 && opt->backward_merge <= 2 &&
-         tri(opt->l2_hints) && opt->cluster_multicast >= -1 && opt->cluster_multicast <= 2 &&
+         tri(opt->l2_hints) && tri(opt->cluster_multicast) &&
          opt->vocab_chunk >= -1;
 }
 
@@ -1277,7 +1224,7 @@ Tuning resolve_tuning(const flce_options* opt) {
   if (opt->backward_merge >= 0) t.merge = opt->backward_merge;
   if (opt->l2_hints >= 0) t.l2_hints = opt->l2_hints != 0;
   if (opt->vocab_chunk >= 0) t.chunk_set = opt->vocab_chunk;
-  if (opt->cluster_multicast >= 0) t.mcast = opt->cluster_multicast;
+  if (opt->cluster_multicast >= 0) t.mcast = opt->cluster_multicast != 0;
   return t;
 }
 
@@ -1340,7 +1287,7 @@ flce_status flce_forward_ex(const void* X, const void* W, const int64_t* labels,
                             float* loss, float* lse, int32_t* valid_count, void* workspace,
                             size_t ws_bytes, int32_t* err_word, void* stream) {
   g_launches = 0;
-  g_quad_launches[0] = g_quad_launches[1] = 0;
+  g_quad_launches = 0;
   if (!options_ok(opt)) return FLCE_ERR_ARG;
   Common c = make_common(X, W, labels, N, H, V, dtype, opt, workspace, ws_bytes, err_word, stream);
   Plan pl;
@@ -1359,7 +1306,7 @@ flce_status flce_backward_ex(const void* X, const void* W, const int64_t* labels
                              const float* grad_loss, void* dX, float* dW, int accumulate_dW,
                              void* workspace, size_t ws_bytes, int32_t* err_word, void* stream) {
   g_launches = 0;
-  g_quad_launches[0] = g_quad_launches[1] = 0;
+  g_quad_launches = 0;
   if (!options_ok(opt)) return FLCE_ERR_ARG;
   Common c = make_common(X, W, labels, N, H, V, dtype, opt, workspace, ws_bytes, err_word, stream);
   Plan pl;
@@ -1380,7 +1327,7 @@ flce_status flce_fwd_bwd_ex(const void* X, const void* W, const int64_t* labels,
                             int32_t* valid_count, void* dX, float* dW, int accumulate_dW,
                             void* workspace, size_t ws_bytes, int32_t* err_word, void* stream) {
   g_launches = 0;
-  g_quad_launches[0] = g_quad_launches[1] = 0;
+  g_quad_launches = 0;
   if (!options_ok(opt)) return FLCE_ERR_ARG;
   Common c = make_common(X, W, labels, N, H, V, dtype, opt, workspace, ws_bytes, err_word, stream);
   Plan pl;
@@ -1461,7 +1408,7 @@ flce_status flce_forward_vocab_shard(const void* X, const void* W_shard, const i
                                      const flce_options* opt, float* partials, void* workspace,
                                      size_t ws_bytes, int32_t* err_word, void* stream) {
   g_launches = 0;
-  g_quad_launches[0] = g_quad_launches[1] = 0;
+  g_quad_launches = 0;
   Common c;
   FLCE_TRY(shard_common(X, W_shard, labels, N, H, V_shard, vocab_offset, vocab_total, dtype, opt,
                         workspace, ws_bytes, err_word, stream, &c));
@@ -1489,7 +1436,7 @@ flce_status flce_combine_vocab_shards(const float* partials, int n_shards, int64
                                       int32_t* valid_count, void* workspace, size_t ws_bytes,
                                       int32_t* err_word, void* stream) {
   g_launches = 0;
-  g_quad_launches[0] = g_quad_launches[1] = 0;
+  g_quad_launches = 0;
   if (!options_ok(opt) || opt->skip_ignored_blocks) return FLCE_ERR_ARG;
   if (n_shards <= 0 || N < 0 || N > (int64_t)INT32_MAX - 1024 || vocab_total <= 0 ||
       vocab_total > (int64_t)INT32_MAX - 1024)
@@ -1535,7 +1482,7 @@ flce_status flce_backward_vocab_shard(const void* X, const void* W_shard, const 
                                       float* dW_shard, int accumulate_dW, void* workspace,
                                       size_t ws_bytes, int32_t* err_word, void* stream) {
   g_launches = 0;
-  g_quad_launches[0] = g_quad_launches[1] = 0;
+  g_quad_launches = 0;
   Common c;
   FLCE_TRY(shard_common(X, W_shard, labels, N, H, V_shard, vocab_offset, vocab_total, dtype, opt,
                         workspace, ws_bytes, err_word, stream, &c));
@@ -1555,7 +1502,7 @@ flce_status flce_backward_vocab_shard(const void* X, const void* W_shard, const 
 flce_status flce_debug_wait_timeout(int32_t* err_word, uint64_t timeout_ns,
                                     int32_t* waited_us, void* stream) {
   g_launches = 0;
-  g_quad_launches[0] = g_quad_launches[1] = 0;
+  g_quad_launches = 0;
   if (!err_word || !waited_us || timeout_ns == 0 || timeout_ns > 10000000000ull)
     return FLCE_ERR_ARG;
   int dev, sms;
@@ -1571,7 +1518,7 @@ flce_status flce_debug_gemm(const void* A, const void* B, float* D, int64_t M, i
                             int64_t K, int a_mn, int b_mn, int accumulate, int32_t* err_word,
                             void* stream) {
   g_launches = 0;
-  g_quad_launches[0] = g_quad_launches[1] = 0;
+  g_quad_launches = 0;
   if (!A || !B || !D || !err_word) return FLCE_ERR_ARG;
   if (M <= 0 || Nn <= 0 || K <= 0 || M > INT32_MAX / 2 || Nn > INT32_MAX / 2 ||
       K > INT32_MAX / 2)
@@ -1599,10 +1546,10 @@ flce_status flce_debug_gemm(const void* A, const void* B, float* D, int64_t M, i
   p.timeout_ns = kTimeoutNs;
   const Walk w = pick_walk(tun, pair, false, p);
   CUtensorMap ta, tb, td;
-  if (a_mn) FLCE_TRY(map_mnmajor(&ta, A, M, K, M, mnmajor_box_k(w, true)));
-  else FLCE_TRY(map_kmajor(&ta, A, K, M, K, kmajor_box(pair, w, true)));
-  if (b_mn) FLCE_TRY(map_mnmajor(&tb, B, Nn, K, Nn, mnmajor_box_k(w, false)));
-  else FLCE_TRY(map_kmajor(&tb, B, K, Nn, K, kmajor_box(pair, w, false)));
+  if (a_mn) FLCE_TRY(map_mnmajor(&ta, A, M, K, M));
+  else FLCE_TRY(map_kmajor(&ta, A, K, M, K, a_box_rows(w)));
+  if (b_mn) FLCE_TRY(map_mnmajor(&tb, B, Nn, K, Nn));
+  else FLCE_TRY(map_kmajor(&tb, B, K, Nn, K, b_box_rows(pair, w)));
   FLCE_TRY(map_f32_out(&td, D, Nn, M, Nn));
   if (!a_mn && !b_mn) return launch_tile<Epi::kStore, false, false>(pair, false, w, dev, sms, ta, tb, td, p, st);
   if (!a_mn && b_mn) return launch_tile<Epi::kStore, false, true>(pair, false, w, dev, sms, ta, tb, td, p, st);

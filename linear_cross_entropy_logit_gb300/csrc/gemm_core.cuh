@@ -404,24 +404,22 @@ __device__ __forceinline__ void staged_store(uint32_t buf, uint8_t* staging, int
   }
 }
 
-// Multicast walks (QUAD): unit u goes to pair (u mod #pairs) as for pairs, and
-// the GROUP consecutive units GROUP*v .. GROUP*v + GROUP-1 -- taken in the same
-// round by the GROUP pairs of one group of 2*GROUP consecutive CTAs -- share an
-// operand: with SHARE_B the same column group g and row blocks GROUP*m + i
-// (groups of row blocks walked like row blocks, bands divided by GROUP);
-// otherwise the same row block and column groups GROUP*h + i (group length 1).
-// The host only launches a multicast walk when these groupings cover the grid
-// exactly.
-template <bool SHARE_B, int GROUP>
+// QUAD launches: unit u goes to pair (u mod #pairs) as for pairs, and units
+// 2v, 2v+1 -- taken by the two pairs of one 4-CTA group in the same round --
+// share an operand: with SHARE_B the same column group g and row blocks
+// 2m, 2m+1 (row-block pairs walked like row blocks, bands halved); otherwise
+// the same row block and column groups 2h, 2h+1 (group length 1).  The host
+// only launches QUAD when these pairings cover the grid exactly.
+template <bool SHARE_B>
 __device__ __forceinline__ void unit_coords_quad(const GemmParams& p, int u, int& mb, int& nb0,
                                                  int& nb1, int& g) {
-  const int i = u % GROUP;
-  const int v = u / GROUP;
+  const int i = u & 1;
+  const int v = u >> 1;
   if constexpr (SHARE_B) {
-    const int mh = p.m_blocks / GROUP;
+    const int mh = p.m_blocks >> 1;
     int mbh;
     if (p.m_fastest) {
-      const int band_h = p.m_band / GROUP;
+      const int band_h = p.m_band >> 1;
       if (band_h > 0 && band_h < mh) {
         const int band_units = band_h * p.n_groups;
         const int band = v / band_units;
@@ -438,10 +436,10 @@ __device__ __forceinline__ void unit_coords_quad(const GemmParams& p, int u, int
       g = v % p.n_groups;
       mbh = v / p.n_groups;
     }
-    mb = GROUP * mbh + i;
+    mb = 2 * mbh + i;
   } else {
-    const int gh = p.n_groups / GROUP;
-    g = GROUP * (v % gh) + i;
+    const int gh = p.n_groups >> 1;
+    g = 2 * (v % gh) + i;
     mb = v / gh;
   }
   nb0 = g * p.group_len;
@@ -454,30 +452,22 @@ __device__ __forceinline__ void unit_coords_quad(const GemmParams& p, int u, int
   }
 }
 
-// One TMA load of a pair-tile operand box, multicast to `mask` when S > 1.
-__device__ __forceinline__ void load_box_quad(uint8_t* dst, const CUtensorMap* map, uint32_t bar,
-                                              int x, int y, uint32_t S, uint16_t mask) {
-  if (S > 1)
-    tma_load_2d_pair_mcast(dst, map, bar, x, y, mask);
-  else
-    tma_load_2d_pair(dst, map, bar, x, y);
-}
-
-// One CTA's 128-row (K-major) or 128-column (MN-major) half of an operand for
-// one k-block.  Not shared: two 8 KB boxes, 64 rows x 64 k (K-major) or 64 MN x
-// 64 k (MN-major).  Shared by the pairs of a group: NP pieces, 2 (GROUP 2: the
-// two boxes above) or 4 (GROUP 4: 32 rows x 64 k, or the k-rows [16q, 16q + 16)
-// of both MN boxes, through maps with those boxes).  With S pairs in this
-// CTA's cluster the CTA loads pieces pic * NP/S .. (pic + 1) * NP/S - 1 and
-// multicasts each to the CTAs of the same pair rank in all S pairs (`mask`);
-// with S = 1 (a 2-CTA cluster) it loads every piece itself.  Every piece keeps
-// its place in the 128-byte-swizzled layout (pieces start on 1 KB boundaries),
-// so the MMA reads the same shared-memory image either way.
-template <bool MN, int GROUP>
+// One CTA's 128-row half of an operand for one k-block, as two 64-row boxes
+// (8 KB each): K-major boxes are 64 rows x 64 k, MN-major boxes 64 MN x 64 k.
+// With `shared` and multicast the CTA loads only box `pic` and multicasts it
+// to itself and its counterpart in the other pair; otherwise both boxes.
+template <bool MN>
 __device__ __forceinline__ void load_half_quad(uint8_t* dst, const CUtensorMap* map, uint32_t bar,
-                                               int row0, int kb, bool shared, uint32_t S,
+                                               int row0, int kb, bool shared, bool mcast,
                                                uint32_t pic, uint16_t mask) {
-  if (!shared) {
+  if (shared && mcast) {
+    const int r = row0 + (int)pic * 64;
+    uint8_t* d = dst + pic * MN_BOX_BYTES;
+    if constexpr (MN)
+      tma_load_2d_pair_mcast(d, map, bar, r, kb * BK, mask);
+    else
+      tma_load_2d_pair_mcast(d, map, bar, kb * BK, r, mask);
+  } else {
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       if constexpr (MN)
@@ -485,32 +475,12 @@ __device__ __forceinline__ void load_half_quad(uint8_t* dst, const CUtensorMap* 
       else
         tma_load_2d_pair(dst + i * MN_BOX_BYTES, map, bar, kb * BK, row0 + i * 64);
     }
-    return;
-  }
-  constexpr int NP = GROUP == 2 ? 2 : 4;
-  const int cnt = NP / (int)S;
-  const int q0 = (int)pic * cnt;
-  for (int q = q0; q < q0 + cnt; ++q) {
-    if constexpr (NP == 2) {
-      if constexpr (MN)
-        load_box_quad(dst + q * MN_BOX_BYTES, map, bar, row0 + q * 64, kb * BK, S, mask);
-      else
-        load_box_quad(dst + q * MN_BOX_BYTES, map, bar, kb * BK, row0 + q * 64, S, mask);
-    } else if constexpr (!MN) {
-      load_box_quad(dst + q * (32 * 128), map, bar, kb * BK, row0 + q * 32, S, mask);
-    } else {
-#pragma unroll
-      for (int bx = 0; bx < 2; ++bx)
-        load_box_quad(dst + bx * MN_BOX_BYTES + q * (16 * 128), map, bar, row0 + bx * 64,
-                      kb * BK + q * 16, S, mask);
-    }
   }
 }
 
-// CL: 1 single-CTA tiles, 2 CTA pairs, 4 CTA pairs walked in groups of GROUP
-// pairs that share an operand by multicast (QUAD; EXT must be false).
-template <Epi EPI, bool A_MN, bool B_MN, int STAGES, int CL, bool EXT, bool SHARE_B = false,
-          int GROUP = 2>
+// CL: 1 single-CTA tiles, 2 CTA pairs, 4 CTA pairs with 4-CTA clusters
+// preferred (QUAD; EXT must be false).
+template <Epi EPI, bool A_MN, bool B_MN, int STAGES, int CL, bool EXT, bool SHARE_B = false>
 __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensorMap& tmB,
                                           const CUtensorMap& tmOut, const GemmParams& p) {
   constexpr bool PAIR = CL >= 2;
@@ -538,15 +508,10 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
   const uint32_t crank = PAIR ? cluster_ctarank() : 0u;  // rank in the cluster
   const uint32_t rank = crank & 1u;   // rank in the pair: 0 = leader (issues the MMAs)
   const uint32_t lrank = crank & ~1u;  // cluster rank of this pair's leader
-  // QUAD: the S pairs of this CTA's cluster share operand pieces by multicast
-  // (S = 1 in a 2-CTA cluster: no multicast); pic = this pair's place in it
-  const uint32_t nct = QUAD ? cluster_nctarank() : (PAIR ? 2u : 1u);
-  const uint32_t S = QUAD ? nct >> 1 : 1u;
-  const bool mcast = S > 1u;
+  // QUAD: multicast only inside a 4-CTA cluster; pic = this pair's place in it
+  const bool mcast = QUAD && cluster_nctarank() == 4u;
   const uint32_t pic = mcast ? (crank >> 1) : 0u;
-  uint16_t mc_mask = 0;  // the CTAs of this pair rank in all S pairs
-  for (uint32_t k = 0; k < S; ++k) mc_mask |= (uint16_t)(1u << (2u * k + rank));
-  const uint16_t all_mask = (uint16_t)((1u << nct) - 1u);
+  const uint16_t mc_mask = (uint16_t)((1u << crank) | (1u << (crank ^ 2u)));
   const uint16_t pair_mask = (uint16_t)(0x3u << lrank);
   const int pair_id = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
   const int num_pairs = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
@@ -554,8 +519,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      // with multicast every pair's MMAs read what this CTA loads
-      mbar_init(&empty[s], mcast ? S : 1u);
+      // with multicast both pairs' MMAs read into this CTA's stages
+      mbar_init(&empty[s], mcast ? 2 : 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
@@ -607,7 +572,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
       for (int u = pair_id; u < us.num_units && ok; u += num_pairs) {
         int mb, nb0, nb1, g;
         if constexpr (QUAD)
-          unit_coords_quad<SHARE_B, GROUP>(p, u, mb, nb0, nb1, g);
+          unit_coords_quad<SHARE_B>(p, u, mb, nb0, nb1, g);
         else
           unit_coords<EXT>(p, us, u, mb, nb0, nb1, g);
         const int a_row = mb * Cfg::TILE_M + (int)rank * BM;
@@ -641,8 +606,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
               // pair multicasts into it -- complete on the leader's barrier.
               const uint32_t bar = mapa_shared(smem_u32(&full[s]), lrank);
               if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * Cfg::STAGE);
-              load_half_quad<A_MN, GROUP>(a_dst, &tmA, bar, a_row, kb, !SHARE_B, S, pic, mc_mask);
-              load_half_quad<B_MN, GROUP>(b_dst, &tmB, bar, b_row, kb, SHARE_B, S, pic, mc_mask);
+              load_half_quad<A_MN>(a_dst, &tmA, bar, a_row, kb, !SHARE_B, mcast, pic, mc_mask);
+              load_half_quad<B_MN>(b_dst, &tmB, bar, b_row, kb, SHARE_B, mcast, pic, mc_mask);
             } else if constexpr (PAIR) {
               // Both CTAs' loads complete on the leader's full barrier, which
               // only the leader arms with the pair's byte count.
@@ -750,7 +715,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
       for (int u = pair_id; u < us.num_units && ok; u += num_pairs) {
         int mb, nb0, nb1, g;
         if constexpr (QUAD)
-          unit_coords_quad<SHARE_B, GROUP>(p, u, mb, nb0, nb1, g);
+          unit_coords_quad<SHARE_B>(p, u, mb, nb0, nb1, g);
         else
           unit_coords<EXT>(p, us, u, mb, nb0, nb1, g);
         for (int nb = nb0; nb < nb1 && ok; ++nb) {
@@ -787,7 +752,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
                 mma_issue(d_tmem, ad, bd, idesc, (ki | kk) != 0 ? 1u : 0u);
             }
             if constexpr (PAIR)
-              mma_commit_pair_multicast(&empty[s], mcast ? all_mask : pair_mask);
+              mma_commit_pair_multicast(&empty[s], mcast ? (uint16_t)0xF : pair_mask);
             else
               mma_commit(&empty[s]);
             ++it;
@@ -823,7 +788,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
     for (int u = pair_id; u < us.num_units && ok; u += num_pairs) {
       int mb, nb0, nb1, g;
       if constexpr (QUAD)
-        unit_coords_quad<SHARE_B, GROUP>(p, u, mb, nb0, nb1, g);
+        unit_coords_quad<SHARE_B>(p, u, mb, nb0, nb1, g);
       else
         unit_coords<EXT>(p, us, u, mb, nb0, nb1, g);
       const int row = mb * Cfg::TILE_M + row_in_tile;
@@ -1013,12 +978,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 
 // CTA pairs without compile-time cluster dimensions: launched with 2-CTA
 // clusters required and 4-CTA clusters preferred (QUAD above).
-template <Epi EPI, bool A_MN, bool B_MN, int STAGES, bool SHARE_B, int GROUP>
+template <Epi EPI, bool A_MN, bool B_MN, int STAGES, bool SHARE_B>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_quad_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmOut, const GemmParams p) {
-  gemm_body<EPI, A_MN, B_MN, STAGES, 4, false, SHARE_B, GROUP>(tmA, tmB, tmOut, p);
+  gemm_body<EPI, A_MN, B_MN, STAGES, 4, false, SHARE_B>(tmA, tmB, tmOut, p);
 }
 
 }  // namespace flce

@@ -32,13 +32,12 @@ WORKLOADS = [("llama3_n8192", 0.0), ("llama3_long_n16384", 0.0), ("qwen25_n16384
 
 def band_edge_rows(N, H, labels, ii):
     """Token rows at the edges of the row-block bands the forward and dZ
-    launches walk (X above 48 MiB is split into ceil(X / 40 MiB) bands, at most
-    4, of 256-row blocks, the band size rounded up to a multiple of four
-    blocks), plus one ignored row inside each band."""
+    launches walk (X above 48 MiB is split into ceil(X / 40 MiB) bands of
+    256-row blocks, at most 4), plus one ignored row inside each band."""
     blocks = -(-N // 256)
     x_bytes = N * H * 2
     bands = min(4, -(-x_bytes // (40 << 20))) if x_bytes > (48 << 20) else 1
-    per = (-(-blocks // bands) + 3) // 4 * 4 * 256
+    per = -(-blocks // bands) * 256
     rows = []
     for b0 in range(0, N, per):
         b1 = min(N, b0 + per)
