@@ -40,6 +40,15 @@ def test_header_exports_all(L):
         assert hasattr(L, n), f"{n} declared in flce.h but not exported"
 
 
+def test_debug_library_exports_all():
+    """The FLCE_DEBUG build exports the same C ABI."""
+    from linear_cross_entropy_logit_gb300 import binding as B
+    D = B.load(B.DEBUG_LIB_PATH)
+    for n in declared_functions():
+        assert hasattr(D, n), f"{n} declared in flce.h but not exported by the debug build"
+    assert D.flce_abi_version() == 106
+
+
 def test_status_strings_and_version(L):
     assert L.flce_abi_version() == 106
     for s in range(8):
