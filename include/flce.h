@@ -92,8 +92,10 @@ size_t flce_workspace_size(int64_t N, int64_t H, int64_t V, flce_dtype dtype, in
 
 /* Vocabulary columns per backward chunk (Cv): the gradient scratch is N x Cv
  * bf16, two such buffers when the merged backward below is enabled.  0 (the
- * default) picks the largest multiple of 256 whose buffers together fit in
- * 256 MiB, clamped to [256, V/2] (one buffer) or [256, V/4] (two buffers);
+ * default) picks the largest multiple of 512 whose buffers together fit in
+ * max(256 MiB, 1024 * V * 2 bytes) -- the bytes of 1024 token rows of bf16
+ * logits, the fully fused chunk of "Fused cross-entropy -- the memory
+ * kernel" -- clamped to [256, V/2] (one buffer) or [256, V/4] (two buffers);
  * with one buffer it is then rounded down to a width whose weight-gradient
  * launch is a whole number of waves of the current device's CTA pairs
  * ((Cv / 256) * ceil(H / 256) a multiple of the pair count) when that keeps at

@@ -45,7 +45,8 @@ namespace {
 constexpr int kStages = 4;       // 1-CTA tiles: 4 x 48 KB stages
 constexpr int kPairStages = 6;   // CTA-pair tiles: 6 x 32 KB stages per CTA
 constexpr int64_t kPartialsBudget = 32ll << 20;   // bytes of forward partials
-constexpr int64_t kDzBudget = 256ll << 20;        // bytes of all dZ chunk buffers (default)
+constexpr int64_t kDzBudgetMin = 256ll << 20;     // bytes of all dZ chunk buffers, at least
+constexpr int64_t kDzRowsEquiv = 1024;            // ... and as many as this many rows of logits
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
 constexpr size_t kAlign = 256;
 
@@ -177,15 +178,25 @@ int64_t wave_aligned(int64_t c, int64_t H) {
   return (a >= 256 && a * 8 >= c * 7) ? a : c;
 }
 
-// Cv: the dZ buffers together take at most kDzBudget (default) and at most
-// half of the N x V logits (each buffer at most V / (2 * buffers) columns); the
-// default width is wave-aligned for the three-launch backward.
+// Bytes the dZ buffers may take together by default: as much as 1024 token
+// rows of bf16 logits over the whole vocabulary -- the fully fused chunk of
+// "Fused cross-entropy -- the memory kernel" (a B*T chunk of 1024 rows, 0.26 GB
+// at V = 128256) -- and at least 256 MiB.  The N x Cv chunk then holds the same
+// bytes as the pages' 1024 x V one, with the roles of tokens and vocabulary
+// swapped.
+int64_t dz_budget(int64_t V) { return std::max<int64_t>(kDzBudgetMin, kDzRowsEquiv * V * 2); }
+
+// Cv: the dZ buffers together take at most dz_budget(V) (default) and at most
+// half of the N x V logits (each buffer at most V / (2 * buffers) columns).
+// The default width is a multiple of 512 (an even number of 256-column blocks,
+// so the weight-gradient launch's row blocks pair up for the multicast walk)
+// and is wave-aligned for the three-launch backward.
 int64_t auto_chunk(int64_t N, int64_t H, int64_t V, const Tuning& t) {
   const int bufs = dz_buffers(t);
   const int64_t half = std::max<int64_t>(256, (V / (2 * bufs)) / 256 * 256);
   const int64_t set = t.chunk_set;
   if (set > 0) return std::min(std::max<int64_t>(ceil_div(set, 256) * 256, 256), half);
-  int64_t c = (kDzBudget / bufs / (std::max<int64_t>(N, 1) * 2)) / 256 * 256;
+  int64_t c = (dz_budget(V) / bufs / (std::max<int64_t>(N, 1) * 2)) / 512 * 512;
   c = std::min(std::max<int64_t>(c, 256), half);
   return merge_planned(t) ? c : wave_aligned(c, H);
 }

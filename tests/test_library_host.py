@@ -69,8 +69,8 @@ def test_workspace_plan_bounded():
         nxv = N * V * 2
         ws = B.flce_workspace_size(N, H, V, B.FLCE_BF16, B.MODE_FWD_BWD)
         # the dZ buffers are the only logit-shaped region: together at most
-        # half of N x V and at most 256 MiB
-        assert bufs * N * cv * 2 <= min(nxv // 2, 256 << 20)
+        # half of N x V and at most the bytes of 1024 rows of logits (or 256 MiB)
+        assert bufs * N * cv * 2 <= min(nxv // 2, max(256 << 20, 1024 * V * 2))
         # whole workspace: dZ buffers + fp32 dX accumulator + forward partials
         assert ws <= bufs * N * cv * 2 + N * H * 4 + (40 << 20)
         assert ws < nxv
@@ -127,20 +127,21 @@ def test_backward_merge_setting():
 
 
 def test_default_chunk_is_wave_aligned_when_close():
-    """With one dZ buffer the default width is rounded down to a multiple of
-    256 * P / gcd(ceil(H/256), P) (P = 76 CTA pairs on a 152-SM GB300, also the
-    value without a device) when that keeps at least 7/8 of the budget width,
-    so the dW launch (Cv/256 x H/256 tiles) is whole waves."""
+    """The budget width is the largest multiple of 512 whose chunk fits
+    max(256 MiB, 1024 rows of bf16 logits over V); with one dZ buffer it is
+    then rounded down to a multiple of 256 * P / gcd(ceil(H/256), P) (P = 76 CTA
+    pairs on a 152-SM GB300, also the value without a device) when that keeps at
+    least 7/8 of it, so the dW launch (Cv/256 x H/256 tiles) is whole waves."""
     import math
     from linear_cross_entropy_logit_gb300 import binding as B
     B.flce_set_vocab_chunk(0)
     assert not B.flce_backward_merge()
     P = 76
     cases = {  # (N, H, V): (budget width, expected)
-        (8192, 4096, 128256): (16384, 14592),   # 57 blocks x 16 = 912 tiles = 12 waves
-        (16384, 4096, 128256): (8192, 8192),    # 4864 would keep only 59%
-        (16384, 3584, 152064): (8192, 8192),    # the aligned step (9728) exceeds the budget
-        (32768, 2304, 256000): (4096, 4096),    # step 19456
+        (8192, 4096, 128256): (16384, 14592),   # 256 MiB; 57 blocks x 16 = 912 tiles = 12 waves
+        (16384, 4096, 128256): (8192, 8192),    # 256 MiB; 4864 would keep only 59%
+        (16384, 3584, 152064): (9216, 9216),    # 1024 rows x V = 311 MB; the step 9728 exceeds it
+        (32768, 2304, 256000): (7680, 7680),    # 1024 rows x V = 524 MB; step 19456
     }
     for (N, H, V), (budget, want) in cases.items():
         cv = B.flce_vocab_chunk(N, H, V)
