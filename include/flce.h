@@ -96,10 +96,10 @@ size_t flce_workspace_size(int64_t N, int64_t H, int64_t V, flce_dtype dtype, in
  * max(256 MiB, 1024 * V * 2 bytes) -- the bytes of 1024 token rows of bf16
  * logits, the fully fused chunk of "Fused cross-entropy -- the memory
  * kernel" -- clamped to [256, V/2] (one buffer) or [256, V/4] (two buffers);
- * with one buffer it is then rounded down to a width whose weight-gradient
- * launch is a whole number of waves of the current device's CTA pairs
- * ((Cv / 256) * ceil(H / 256) a multiple of the pair count) when that keeps at
- * least 7/8 of it.  A set value is rounded up to a multiple of 256 and
+ * with one buffer it is then narrowed, by at most 1/8, to the width whose
+ * weight-gradient launch ((Cv / 256) * ceil(H / 256) tiles) best fills its
+ * last wave of the current device's CTA pairs (a multiple of 512 when
+ * ceil(H / 256) is odd).  A set value is rounded up to a multiple of 256 and
  * clamped the same way.  Process-wide default of the calls whose options leave
  * vocab_chunk at -1 (the plain calls always use it); set it before sizing
  * workspaces.  flce_vocab_chunk returns the width such a call of this shape

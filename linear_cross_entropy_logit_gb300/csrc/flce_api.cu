@@ -166,16 +166,31 @@ int64_t device_pairs() {
 }
 
 // Three-launch backward: the dW launch of a chunk has (Cv / 256) x ceil(H / 256)
-// tiles; when that is a whole number of waves of CTA pairs no launch ends on a
-// partial wave.  The width is rounded down to such a multiple when that keeps
-// at least 7/8 of it (Llama-3 shape: 16384 -> 14592, 12 waves; measured 2.6%
-// faster dW launches and slightly faster steps on a GB300).
-int64_t wave_aligned(int64_t c, int64_t H) {
+// tiles, whose last wave of CTA pairs is partly idle unless the count is a
+// whole number of waves.  Among the widths that keep at least 7/8 of the
+// budget width -- multiples of 256, of 512 when ceil(H / 256) is odd (so the
+// dW launch's row blocks pair up for the multicast walk) -- the one whose dW
+// launch fills its last wave best is taken (the widest within half a point
+// of the best), but the widest width stays unless that best fill beats its
+// fill by 2.5 points.  Measured on a GB300: Llama-3 shape 16384 ->
+// 14592 (912 tiles, 12 whole waves; 2.6% faster dW launches); Qwen-2.5 shape
+// 9216 -> 8192 (dW at 9216 ran 2.5% slower, its last wave 95% full against 98%).
+int64_t wave_fit(int64_t c, int64_t H) {
   const int64_t pairs = device_pairs();
   const int64_t hb = ceil_div(H, BN);
-  const int64_t step = 256 * (pairs / std::gcd(hb, pairs));
-  const int64_t a = c / step * step;
-  return (a >= 256 && a * 8 >= c * 7) ? a : c;
+  const int64_t unit = (hb % 2) ? 512 : 256;
+  auto fill = [&](int64_t w) {
+    const int64_t tiles = (w / 256) * hb;
+    return (double)tiles / (double)(ceil_div(tiles, pairs) * pairs);
+  };
+  const int64_t widest = c / unit * unit;
+  if (widest < unit) return std::max<int64_t>(256, c / 256 * 256);
+  double top = 0.0;
+  for (int64_t w = widest; w >= unit && w * 8 >= c * 7; w -= unit) top = std::max(top, fill(w));
+  if (top <= fill(widest) + 0.025) return widest;
+  for (int64_t w = widest; w >= unit && w * 8 >= c * 7; w -= unit)
+    if (fill(w) >= top - 0.005) return w;
+  return widest;
 }
 
 // Bytes the dZ buffers may take together by default: as much as 1024 token
@@ -198,7 +213,7 @@ int64_t auto_chunk(int64_t N, int64_t H, int64_t V, const Tuning& t) {
   if (set > 0) return std::min(std::max<int64_t>(ceil_div(set, 256) * 256, 256), half);
   int64_t c = (dz_budget(V) / bufs / (std::max<int64_t>(N, 1) * 2)) / 512 * 512;
   c = std::min(std::max<int64_t>(c, 256), half);
-  return merge_planned(t) ? c : wave_aligned(c, H);
+  return merge_planned(t) ? c : wave_fit(c, H);
 }
 
 bool make_plan(int64_t N, int64_t H, int64_t V, flce_dtype dtype, int mode, const Tuning& t,
