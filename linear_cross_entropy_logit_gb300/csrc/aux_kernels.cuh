@@ -9,16 +9,63 @@
 namespace flce {
 
 constexpr int MERGE_THREADS = 256;
+constexpr int MERGE_ROWS = 32;                             // token rows per merge block
+constexpr int MERGE_SLICES = MERGE_THREADS / MERGE_ROWS;  // warps, each over a slice of the groups
 constexpr float LN2 = 0.6931471805599453f;
 
-// One thread per token row.  Merges the vocabulary-group partials
+// Blocks of the merge kernels for N token rows.
+inline int64_t merge_block_count(int64_t N) {
+  return ((N > 0 ? N : 1) + MERGE_ROWS - 1) / MERGE_ROWS;
+}
+
+// One slice of one row's vocabulary-group partials: groups slice,
+// slice + MERGE_SLICES, ... merged online into (max*log2e, sum rescaled to
+// that max, target logit, logit sum).  A group with no column (-inf max)
+// adds nothing to the sum.
+__device__ __forceinline__ float4 merge_slice(const float4* __restrict__ partials, int n_groups,
+                                              int m_pad, int row, int slice) {
+  float m = -INFINITY, s = 0.f, zy = 0.f, zs = 0.f;
+#pragma unroll 4
+  for (int g = slice; g < n_groups; g += MERGE_SLICES) {
+    const float4 q = partials[(size_t)g * m_pad + row];
+    if (q.x > m) {
+      s = s * ex2_approx(m - q.x) + q.y;
+      m = q.x;
+    } else if (q.x > -INFINITY) {
+      s += q.y * ex2_approx(q.x - m);
+    }
+    zy += q.z;
+    zs += q.w;
+  }
+  return make_float4(m, s, zy, zs);
+}
+
+// The MERGE_SLICES slice results of row r, combined in slice order.
+__device__ __forceinline__ float4 combine_slices(const float4 (*part)[MERGE_ROWS], int r) {
+  float M = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < MERGE_SLICES; ++k) M = fmaxf(M, part[k][r].x);
+  float S = 0.f, zy = 0.f, zs = 0.f;
+#pragma unroll
+  for (int k = 0; k < MERGE_SLICES; ++k) {
+    const float4 q = part[k][r];
+    if (q.x > -INFINITY) S += q.y * ex2_approx(q.x - M);
+    zy += q.z;
+    zs += q.w;
+  }
+  return make_float4(M, S, zy, zs);
+}
+
+// MERGE_ROWS token rows per block; warp k merges groups k, k + MERGE_SLICES,
+// ... of every row (coalesced: a warp reads 32 consecutive rows of one group),
+// warp 0 combines the slices.  Merges the vocabulary-group partials
 // (max*log2e, rescaled exp-sum, target logit, logit sum) into
 //   lse_i = m_i + log d_i       ("Chunked and Fused Cross-Entropy ...",
 //                                 "Mathematical Mechanics ...", step 2)
 //   l_i   = valid_i * (lse_i - (1-eps) z_{i,y_i} - (eps/V) sum_j z_ij
 //                    + alpha lse_i^2)            (z-loss term when alpha > 0)
 // writes l_i per row when asked, and reduces l_i and valid_i over the block in
-// a fixed tree order.
+// a fixed tree order.  Every order is fixed, so the results are deterministic.
 // A label outside [0, V) that is not ignore_index sets FLCE_ERR_LABEL and
 // the row counts as ignored.
 static __global__ void __launch_bounds__(MERGE_THREADS)
@@ -27,26 +74,23 @@ static __global__ void __launch_bounds__(MERGE_THREADS)
                      float z_loss, float* __restrict__ lse_out, float* __restrict__ row_loss,
                      double* __restrict__ block_loss, int* __restrict__ block_valid,
                      int* err_word, const int* __restrict__ block_active, int block_rows) {
-  __shared__ double s_loss[MERGE_THREADS];
-  __shared__ int s_valid[MERGE_THREADS];
-  const int row = blockIdx.x * MERGE_THREADS + threadIdx.x;
+  __shared__ float4 s_part[MERGE_SLICES][MERGE_ROWS];
+  const int r = threadIdx.x % MERGE_ROWS;
+  const int slice = threadIdx.x / MERGE_ROWS;
+  const int row = blockIdx.x * MERGE_ROWS + r;
+  // a skipped block: every label in it is ignore_index, its logits were not formed
+  const bool skipped = row < N && block_active && !block_active[row / block_rows];
+  if (row < N && !skipped) s_part[slice][r] = merge_slice(partials, n_groups, m_pad, row, slice);
+  __syncthreads();
+  if (slice != 0) return;
   double loss = 0.0;
   int valid = 0;
-  if (row < N && block_active && !block_active[row / block_rows]) {
-    // a skipped block: every label in it is ignore_index, its logits were not formed
+  if (skipped) {
     lse_out[row] = __int_as_float(0x7fc00000);
     if (row_loss) row_loss[row] = 0.f;
   } else if (row < N) {
-    float M = -INFINITY;
-    for (int g = 0; g < n_groups; ++g) M = fmaxf(M, partials[(size_t)g * m_pad + row].x);
-    float S = 0.f, zy = 0.f, zs = 0.f;
-    for (int g = 0; g < n_groups; ++g) {
-      const float4 q = partials[(size_t)g * m_pad + row];
-      S += q.y * ex2_approx(q.x - M);
-      zy += q.z;
-      zs += q.w;
-    }
-    const float lse = (M + log2f(S)) * LN2;
+    const float4 t = combine_slices(s_part, r);
+    const float lse = (t.x + log2f(t.y)) * LN2;
     lse_out[row] = lse;
     const long long y = labels[row];
     if (y != ignore_index) {
@@ -54,48 +98,39 @@ static __global__ void __launch_bounds__(MERGE_THREADS)
         record_error(err_word, kErrLabel);
       } else {
         valid = 1;
-        double l = (double)lse - (1.0 - (double)smoothing) * (double)zy;
-        if (smoothing != 0.f) l -= (double)smoothing / (double)V * (double)zs;
+        double l = (double)lse - (1.0 - (double)smoothing) * (double)t.z;
+        if (smoothing != 0.f) l -= (double)smoothing / (double)V * (double)t.w;
         if (z_loss != 0.f) l += (double)z_loss * (double)lse * (double)lse;
         loss = l;
       }
     }
     if (row_loss) row_loss[row] = (float)loss;
   }
-  s_loss[threadIdx.x] = loss;
-  s_valid[threadIdx.x] = valid;
-  __syncthreads();
-  for (int w = MERGE_THREADS / 2; w > 0; w >>= 1) {
-    if (threadIdx.x < w) {
-      s_loss[threadIdx.x] += s_loss[threadIdx.x + w];
-      s_valid[threadIdx.x] += s_valid[threadIdx.x + w];
-    }
-    __syncthreads();
+#pragma unroll
+  for (int o = MERGE_ROWS / 2; o > 0; o >>= 1) {
+    loss += __shfl_xor_sync(0xffffffffu, loss, o);
+    valid += __shfl_xor_sync(0xffffffffu, valid, o);
   }
-  if (threadIdx.x == 0) {
-    block_loss[blockIdx.x] = s_loss[0];
-    block_valid[blockIdx.x] = s_valid[0];
+  if (r == 0) {
+    block_loss[blockIdx.x] = loss;
+    block_valid[blockIdx.x] = valid;
   }
 }
 
-// One thread per token row: merge the vocabulary-group partials of ONE
-// vocabulary shard into a single (max*log2e, rescaled sum, z_y, sum_z) per
-// row -- the statistic shards exchange in the vocabulary-parallel layout.
+// Merge the vocabulary-group partials of ONE vocabulary shard into a single
+// (max*log2e, rescaled sum, z_y, sum_z) per row -- the statistic shards
+// exchange in the vocabulary-parallel layout.  Same geometry as
+// lse_merge_kernel.
 static __global__ void __launch_bounds__(MERGE_THREADS)
     shard_partial_kernel(const float4* __restrict__ partials, int n_groups, int m_pad, int N,
                          float4* __restrict__ out) {
-  const int row = blockIdx.x * MERGE_THREADS + threadIdx.x;
-  if (row >= N) return;
-  float M = -INFINITY;
-  for (int g = 0; g < n_groups; ++g) M = fmaxf(M, partials[(size_t)g * m_pad + row].x);
-  float S = 0.f, zy = 0.f, zs = 0.f;
-  for (int g = 0; g < n_groups; ++g) {
-    const float4 q = partials[(size_t)g * m_pad + row];
-    S += q.y * ex2_approx(q.x - M);
-    zy += q.z;
-    zs += q.w;
-  }
-  out[row] = make_float4(M, S, zy, zs);
+  __shared__ float4 s_part[MERGE_SLICES][MERGE_ROWS];
+  const int r = threadIdx.x % MERGE_ROWS;
+  const int slice = threadIdx.x / MERGE_ROWS;
+  const int row = blockIdx.x * MERGE_ROWS + r;
+  if (row < N) s_part[slice][r] = merge_slice(partials, n_groups, m_pad, row, slice);
+  __syncthreads();
+  if (slice == 0 && row < N) out[row] = combine_slices(s_part, r);
 }
 
 // Single block: fixed-order sum of the block partials, then the mean over
@@ -144,24 +179,50 @@ static __global__ void grad_scale_kernel(const int* valid_count, const float* gr
   *scale_out = c;
 }
 
-// dX = bf16(dX_acc), round to nearest even; n4 = number of float4 groups.
-static __global__ void dx_finalize_bf16_kernel(const float4* __restrict__ acc, uint2* __restrict__ out,
-                                        size_t n4) {
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4;
-       i += (size_t)gridDim.x * blockDim.x) {
-    const float4 v = acc[i];
-    out[i] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+// fp32 -> bf16 (round to nearest even) of n4 float4 groups: every thread
+// issues CONVERT_UNROLL independent 16-byte loads before its stores, so a
+// launch of a few blocks per SM keeps enough reads in flight to stream at
+// HBM speed.  The source is read once (evict-first loads).
+constexpr int CONVERT_THREADS = 256;
+constexpr int CONVERT_UNROLL = 4;
+
+__device__ __forceinline__ void convert_f32_bf16(const float4* __restrict__ in,
+                                                 uint2* __restrict__ out, size_t n4) {
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t i0 = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i0 < n4;
+       i0 += stride * CONVERT_UNROLL) {
+    float4 v[CONVERT_UNROLL];
+#pragma unroll
+    for (int u = 0; u < CONVERT_UNROLL; ++u) {
+      const size_t i = i0 + u * stride;
+      if (i < n4) v[u] = __ldcs(in + i);
+    }
+#pragma unroll
+    for (int u = 0; u < CONVERT_UNROLL; ++u) {
+      const size_t i = i0 + u * stride;
+      if (i < n4) out[i] = make_uint2(pack_bf16x2(v[u].x, v[u].y), pack_bf16x2(v[u].z, v[u].w));
+    }
   }
 }
 
-// fp32 -> bf16 (round to nearest even), n4 = number of float4 groups.
-static __global__ void cast_f32_bf16_kernel(const float4* __restrict__ in, uint2* __restrict__ out,
-                                     size_t n4) {
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4;
-       i += (size_t)gridDim.x * blockDim.x) {
-    const float4 v = in[i];
-    out[i] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
-  }
+// Blocks of a conversion launch over n4 float4 groups on `sms` SMs.
+inline unsigned convert_blocks(size_t n4, int sms) {
+  const size_t per_block = (size_t)CONVERT_THREADS * CONVERT_UNROLL;
+  const size_t want = (n4 + per_block - 1) / per_block;
+  const size_t cap = (size_t)(sms > 0 ? sms : 1) * 8;
+  return (unsigned)(want < 1 ? 1 : (want < cap ? want : cap));
+}
+
+// dX = bf16(dX_acc).
+static __global__ void __launch_bounds__(CONVERT_THREADS)
+    dx_finalize_bf16_kernel(const float4* __restrict__ acc, uint2* __restrict__ out, size_t n4) {
+  convert_f32_bf16(acc, out, n4);
+}
+
+// fp32 inputs -> bf16 operands.
+static __global__ void __launch_bounds__(CONVERT_THREADS)
+    cast_f32_bf16_kernel(const float4* __restrict__ in, uint2* __restrict__ out, size_t n4) {
+  convert_f32_bf16(in, out, n4);
 }
 
 // Token blocks of `block_rows` rows that hold at least one label other than

@@ -232,7 +232,7 @@ bool make_plan(int64_t N, int64_t H, int64_t V, flce_dtype dtype, int mode, cons
   while ((int64_t)ceil_div(p.v_tiles, L) * p.m_pad * 16 > kPartialsBudget && L < p.v_tiles) L *= 2;
   p.group_len = L;
   p.n_groups = (int)ceil_div(p.v_tiles, L);
-  p.merge_blocks = (int)ceil_div(std::max<int64_t>(N, 1), MERGE_THREADS);
+  p.merge_blocks = (int)merge_block_count(N);
   p.chunk = auto_chunk(N, H, V, t);
   p.n_chunks = (int)ceil_div(V, p.chunk);
   p.dz_bufs = dz_buffers(t);
@@ -725,7 +725,8 @@ flce_status build_skip_lists(const Common& c, const Plan& pl, bool pair, SkipLis
 }
 
 // fp32 inputs: one rounding to bf16 into the workspace.
-flce_status cast_inputs(const Common& c, const Plan& pl, const void** Xb, const void** Wb) {
+flce_status cast_inputs(const Common& c, const Plan& pl, int sms, const void** Xb,
+                        const void** Wb) {
   if (c.dtype == FLCE_BF16) {
     *Xb = c.X;
     *Wb = c.W;
@@ -736,12 +737,12 @@ flce_status cast_inputs(const Common& c, const Plan& pl, const void** Xb, const 
   void* wo = ws + pl.off_wcast;
   const size_t nx4 = (size_t)c.N * c.H / 4, nw4 = (size_t)c.V * c.H / 4;
   if (nx4) {
-    cast_f32_bf16_kernel<<<(unsigned)std::min<size_t>(ceil_div(nx4, 256), 4096), 256, 0, c.st>>>(
+    cast_f32_bf16_kernel<<<convert_blocks(nx4, sms), CONVERT_THREADS, 0, c.st>>>(
         static_cast<const float4*>(c.X), static_cast<uint2*>(xo), nx4);
     ++g_launches;
     FLCE_CUDA(cudaGetLastError());
   }
-  cast_f32_bf16_kernel<<<(unsigned)std::min<size_t>(ceil_div(nw4, 256), 4096), 256, 0, c.st>>>(
+  cast_f32_bf16_kernel<<<convert_blocks(nw4, sms), CONVERT_THREADS, 0, c.st>>>(
       static_cast<const float4*>(c.W), static_cast<uint2*>(wo), nw4);
   ++g_launches;
   FLCE_CUDA(cudaGetLastError());
@@ -1091,9 +1092,8 @@ flce_status run_backward(const Common& c, const Plan& pl, int dev, int sms, cons
   }
   if (c.dtype == FLCE_BF16 && !c.dx_partial_f32) {
     const size_t n4 = (size_t)N * H / 4;
-    dx_finalize_bf16_kernel<<<(unsigned)std::min<size_t>(ceil_div(n4, 256), 2 * sms), 256, 0,
-                              c.st>>>(reinterpret_cast<const float4*>(dx_acc),
-                                      static_cast<uint2*>(dX), n4);
+    dx_finalize_bf16_kernel<<<convert_blocks(n4, sms), CONVERT_THREADS, 0, c.st>>>(
+        reinterpret_cast<const float4*>(dx_acc), static_cast<uint2*>(dX), n4);
     ++g_launches;
     FLCE_CUDA(cudaGetLastError());
   }
@@ -1322,7 +1322,7 @@ flce_status flce_forward_ex(const void* X, const void* W, const int64_t* labels,
   int dev, sms;
   FLCE_TRY(device_check(&dev, &sms));
   const void *Xb, *Wb;
-  FLCE_TRY(cast_inputs(c, pl, &Xb, &Wb));
+  FLCE_TRY(cast_inputs(c, pl, sms, &Xb, &Wb));
   return run_forward(c, pl, dev, sms, Xb, Wb, loss, lse, valid_count);
 }
 
@@ -1342,7 +1342,7 @@ flce_status flce_backward_ex(const void* X, const void* W, const int64_t* labels
   int dev, sms;
   FLCE_TRY(device_check(&dev, &sms));
   const void *Xb, *Wb;
-  FLCE_TRY(cast_inputs(c, pl, &Xb, &Wb));
+  FLCE_TRY(cast_inputs(c, pl, sms, &Xb, &Wb));
   return run_backward(c, pl, dev, sms, Xb, Wb, lse, valid_count, grad_loss, dX, dW,
                       accumulate_dW);
 }
@@ -1363,7 +1363,7 @@ flce_status flce_fwd_bwd_ex(const void* X, const void* W, const int64_t* labels,
   int dev, sms;
   FLCE_TRY(device_check(&dev, &sms));
   const void *Xb, *Wb;
-  FLCE_TRY(cast_inputs(c, pl, &Xb, &Wb));
+  FLCE_TRY(cast_inputs(c, pl, sms, &Xb, &Wb));
   FLCE_TRY(run_forward(c, pl, dev, sms, Xb, Wb, loss, lse, valid_count));
   return run_backward(c, pl, dev, sms, Xb, Wb, lse, valid_count, grad_loss, dX, dW,
                       accumulate_dW);
@@ -1445,14 +1445,14 @@ flce_status flce_forward_vocab_shard(const void* X, const void* W_shard, const i
   int dev, sms;
   FLCE_TRY(device_check(&dev, &sms));
   const void *Xb, *Wb;
-  FLCE_TRY(cast_inputs(c, pl, &Xb, &Wb));
+  FLCE_TRY(cast_inputs(c, pl, sms, &Xb, &Wb));
   return run_forward(c, pl, dev, sms, Xb, Wb, nullptr, nullptr, nullptr,
                      reinterpret_cast<float4*>(partials));
 }
 
 size_t flce_combine_workspace_size(int64_t N) {
   if (N < 0) return 0;
-  const size_t nb = (size_t)ceil_div(std::max<int64_t>(N, 1), MERGE_THREADS);
+  const size_t nb = (size_t)merge_block_count(N);
   return align_up(nb * sizeof(double), kAlign) + align_up(nb * sizeof(int), kAlign);
 }
 
@@ -1478,7 +1478,7 @@ flce_status flce_combine_vocab_shards(const float* partials, int n_shards, int64
   int dev, sms;
   FLCE_TRY(device_check(&dev, &sms));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int nb = (int)ceil_div(std::max<int64_t>(N, 1), MERGE_THREADS);
+  const int nb = (int)merge_block_count(N);
   double* block_loss = static_cast<double*>(workspace);
   int* block_valid = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) +
                                             align_up(nb * sizeof(double), kAlign));
@@ -1520,7 +1520,7 @@ flce_status flce_backward_vocab_shard(const void* X, const void* W_shard, const 
   int dev, sms;
   FLCE_TRY(device_check(&dev, &sms));
   const void *Xb, *Wb;
-  FLCE_TRY(cast_inputs(c, pl, &Xb, &Wb));
+  FLCE_TRY(cast_inputs(c, pl, sms, &Xb, &Wb));
   return run_backward(c, pl, dev, sms, Xb, Wb, lse, valid_count, grad_loss, dX_partial, dW_shard,
                       accumulate_dW);
 }

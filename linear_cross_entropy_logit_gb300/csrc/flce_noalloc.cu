@@ -76,7 +76,7 @@ bool na_plan(int64_t N, int64_t V, NaPlan* p) {
   p->m_blocks = (int)na_ceil_div(std::max<int64_t>(N, 1), BM);
   p->m_pad = p->m_blocks * BM;
   p->v_tiles = (int)na_ceil_div(V, BN);
-  p->merge_blocks = (int)na_ceil_div(std::max<int64_t>(N, 1), MERGE_THREADS);
+  p->merge_blocks = (int)merge_block_count(N);
   const size_t sums = na_align((size_t)p->merge_blocks * sizeof(double)) +
                       na_align((size_t)p->merge_blocks * sizeof(int));
   for (int L = 1;; L *= 2) {
