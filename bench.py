@@ -36,7 +36,7 @@ DEFAULT_WORKLOAD = "llama3_n8192"
 def parse_args():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=150)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
@@ -202,6 +202,24 @@ def peaks():
                 "source": "fallback"}
 
 
+# The sustained bf16 figure is a cuBLAS GEMM run back to back for seconds
+# under the power cap; the burst figure a short best-of-ten.  A timed loop at
+# least this long has settled under the cap like the sustained loop, so it is
+# stated against that figure; a shorter one against the burst figure.
+SUSTAINED_LOOP_S = 2.0
+
+
+def peak_choice(pk: dict, wall_s: float):
+    """(name, TFLOP/s, reason) of the bf16 peak a timed loop of wall_s seconds
+    is stated against."""
+    if wall_s >= SUSTAINED_LOOP_S:
+        return ("sustained", pk["bf16_sustained"],
+                f"at least {SUSTAINED_LOOP_S:g} s of back-to-back work under the power cap, "
+                "like the sustained figure's own loop")
+    return ("burst", pk["bf16_burst"],
+            f"shorter than {SUSTAINED_LOOP_S:g} s, so the clock has not settled under the cap")
+
+
 # ----------------------------------------------------------------------------
 # Clock sampling during the timed region
 # ----------------------------------------------------------------------------
@@ -256,13 +274,13 @@ class ClockSampler:
 # ----------------------------------------------------------------------------
 # Reference arm: the fp64 oracle on the host cores
 # ----------------------------------------------------------------------------
-def oracle_sample(wl, rows: int):
+def oracle_sample(wl, rows: int, z_loss: float = 0.0):
     """The oracle's fused forward+backward on the first ``rows`` tokens."""
     from oracle import flce_oracle as O
     r = min(rows, wl.N)
     t0 = time.perf_counter()
     O.fwd_bwd(wl.x[:r], wl.w, wl.labels[:r], wl.spec.ignore_index, wl.spec.smoothing,
-              wl.spec.reduction)
+              wl.spec.reduction, z_loss=z_loss)
     return r, time.perf_counter() - t0
 
 
@@ -273,10 +291,10 @@ def run_reference(args, rank: int):
     spec = workload_spec(args)
     wl = I.make_workload(spec, seed=args.seed)
     for _ in range(args.warmup):
-        oracle_sample(wl, args.reference_rows)
+        oracle_sample(wl, args.reference_rows, args.z_loss)
     total_rows, total_s = 0, 0.0
     for _ in range(args.steps):
-        r, dt = oracle_sample(wl, args.reference_rows)
+        r, dt = oracle_sample(wl, args.reference_rows, args.z_loss)
         total_rows += r
         total_s += dt
     value = total_rows / total_s
@@ -288,7 +306,7 @@ def run_reference(args, rank: int):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(spec, None),
+        "config": line_config(spec, args, args.gpus),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -343,7 +361,7 @@ def backward_layout(mode, args) -> str:
     return "dZ(c) launch, then one merged dW(c) + dX(c) launch per vocabulary chunk"
 
 
-def workload_config(spec, chunk):
+def workload_config(spec):
     cfg = {"workload": spec.name, "N": spec.N, "H": spec.H, "V": spec.V,
            "inputs": f"X {spec.dtype} N(0,{spec.x_std}^2)"
                      + (" RMS-normed rows" if spec.x_rms_rows else "")
@@ -353,8 +371,18 @@ def workload_config(spec, chunk):
                      + f", labels {spec.labels}",
            "ignored_tokens": spec.n_ignore, "ignore_index": spec.ignore_index,
            "smoothing": spec.smoothing, "reduction": spec.reduction}
-    if chunk is not None:
-        cfg["vocab_chunk"] = chunk
+    return cfg
+
+
+def line_config(spec, args, world: int):
+    """The JSON line's `config`: the workload alone, the same on both arms
+    (how our engine runs it goes under `engine`)."""
+    elem = 2 if spec.dtype == "bf16" else 4
+    cfg = workload_config(spec)
+    cfg["l2"] = "inputs larger than L2 (W alone is %.2f GB)" % (spec.V * spec.H * elem / 1e9)
+    cfg["parallelism"] = f"replicas x{world} (each rank its own batch, no collective)"
+    if args.z_loss:
+        cfg["z_loss"] = args.z_loss
     return cfg
 
 
@@ -613,15 +641,14 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     # algorithmic bytes of one step: X, W read; dX, dW written; labels, lse
     elem = 2 if spec.dtype == "bf16" else 4
     bytes_step = N * H * elem * 2 + V * H * elem + V * H * 4 + N * 8 + N * 4
-    # Peaks: every GEMM kind is timed per launch (~0.5 ms at the Llama-3 shape)
-    # inside a loop of about a second, so the burst figure is the one that
-    # applies; the fraction of the sustained (seconds-long, power-capped)
-    # figure is printed beside it.
-    t_tensor = flops_step / (pk["bf16_burst"] * 1e12)
+    # Peaks: the stated one follows the length of the timed loop (see
+    # peak_choice); the fractions of both measured figures are printed.
+    pname, pval, pwhy = peak_choice(pk, wall)
     t_hbm = bytes_step / (pk["hbm_gbs"] * 1e9)
+    t_tensor = flops_step / (pval * 1e12)
     step_frac = max(t_tensor, t_hbm) / (ms_per_step / 1e3)
-    t_tensor_sus = flops_step / (pk["bf16_sustained"] * 1e12)
-    step_frac_sus = max(t_tensor_sus, t_hbm) / (ms_per_step / 1e3)
+    step_frac_burst = max(flops_step / (pk["bf16_burst"] * 1e12), t_hbm) / (ms_per_step / 1e3)
+    step_frac_sus = max(flops_step / (pk["bf16_sustained"] * 1e12), t_hbm) / (ms_per_step / 1e3)
 
     # dominant kernel: largest share of the profiled device time
     kinds = {}
@@ -645,19 +672,21 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     if dom:
         ach = kinds[dom]["tflops"]
         src = "measured (MEASURED_PEAKS.json)" if pk["source"] == "measured" else "fallback"
-        roofline = {"bound": "tensor", "achieved": ach, "peak": pk["bf16_burst"],
-                    "unit": "TFLOP/s", "frac": ach / pk["bf16_burst"],
+        roofline = {"bound": "tensor", "achieved": ach, "peak": pval,
+                    "unit": "TFLOP/s", "frac": ach / pval,
                     "traffic": traffic.get(dom) if traffic else None,
                     "kernel": dom,
-                    "peak_source": f"{src} bf16 burst: the kernel is timed per launch "
+                    "peak_source": f"{src} bf16 {pname}: the kernel is timed per launch "
                                    f"({kinds[dom]['ms_per_launch']:.3f} ms) inside a "
-                                   f"{wall:.2f} s loop",
+                                   f"{wall:.2f} s loop of back-to-back steps; {pwhy}",
+                    "peak_burst": pk["bf16_burst"],
+                    "frac_of_burst": ach / pk["bf16_burst"],
                     "peak_sustained": pk["bf16_sustained"],
                     "frac_of_sustained": ach / pk["bf16_sustained"]}
 
     cpu = None
     if args.cpu_baseline_rows > 0 and world == 1:
-        r, secs = oracle_sample(wl, args.cpu_baseline_rows)
+        r, secs = oracle_sample(wl, args.cpu_baseline_rows, args.z_loss)
         cpu = {"value": r / secs, "unit": "tokens/s", "cores": host_cores(), "kind": "oracle",
                "sample": f"first {r} of {N} tokens, full V={V} and H={H}, fp64 oracle "
                          f"forward+backward (numpy float64 matmul), {secs:.1f} s"}
@@ -673,24 +702,24 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": spec.dtype, "data": "synthetic",
-        "config": dict(workload_config(spec, chunk),
-                       l2="inputs larger than L2 (W alone is %.2f GB)" % (V * H * elem / 1e9),
-                       parallelism=f"replicas x{world} (each rank its own batch, no collective)",
-                       tiles="128x256 single CTA" if args.single_cta else "256x256 CTA pair",
-                       cluster_multicast=(not args.single_cta) and B.flce_cluster_multicast(),
-                       backward=backward_layout(merge_mode, args),
-                       z_loss=args.z_loss,
-                       skip_ignored_blocks=args.skip_ignored,
-                       grad_filter=args.grad_filter or None,
-                       vocab_shards=args.vocab_shards or None,
-                       l2_hints=args.l2_hints),
+        "config": line_config(spec, args, world),
+        "engine": {"vocab_chunk": chunk,
+                   "tiles": "128x256 single CTA" if args.single_cta else "256x256 CTA pair",
+                   "cluster_multicast": (not args.single_cta) and B.flce_cluster_multicast(),
+                   "backward": backward_layout(merge_mode, args),
+                   "skip_ignored_blocks": args.skip_ignored,
+                   "grad_filter": args.grad_filter or None,
+                   "vocab_shards": args.vocab_shards or None,
+                   "l2_hints": args.l2_hints},
         "tflops": tflops,
         "skip": skip_info,
         "tflops_executed": tflops * skip_info["active_token_fraction"] if skip_info else tflops,
         "step_roofline": {"bound": "tensor" if t_tensor >= t_hbm else "hbm",
                           "frac": step_frac, "flops": flops_step, "bytes": bytes_step,
-                          "peak_tflops": pk["bf16_burst"],
-                          "peak_source": f"{pk['source']} bf16 burst",
+                          "peak_tflops": pval,
+                          "peak_source": f"{pk['source']} bf16 {pname}",
+                          "frac_of_burst": step_frac_burst,
+                          "peak_tflops_burst": pk["bf16_burst"],
                           "frac_of_sustained": step_frac_sus,
                           "peak_tflops_sustained": pk["bf16_sustained"]},
         "roofline": roofline,

@@ -128,3 +128,29 @@ def test_peaks_measured_and_fallback(bench, tmp_path, monkeypatch):
     p = bench.peaks()
     assert p == {"bf16_burst": 1899.8, "bf16_sustained": 1728.5, "hbm_gbs": 6695.5,
                  "source": "measured"}
+
+
+def test_peak_choice_follows_the_timed_loop(bench):
+    pk = {"bf16_burst": 1900.0, "bf16_sustained": 1700.0, "hbm_gbs": 6800.0}
+    name, val, why = bench.peak_choice(pk, 0.4)
+    assert (name, val) == ("burst", 1900.0) and why
+    name, val, why = bench.peak_choice(pk, bench.SUSTAINED_LOOP_S)
+    assert (name, val) == ("sustained", 1700.0) and why
+    name, _, _ = bench.peak_choice(pk, 3.0)
+    assert name == "sustained"
+
+
+def test_reference_arm_prints_the_same_config(bench, capsys):
+    """The reference arm's `config` is built by the same function as ours: the
+    workload alone, no engine settings."""
+    import json
+    a = types.SimpleNamespace(workload="llama3_n8192", shape="64,32,256", seed=0, steps=1,
+                              warmup=0, reference_rows=8, gpus=1, z_loss=0.0)
+    bench.run_reference(a, 0)
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    want = bench.line_config(bench.workload_spec(a), a, 1)
+    assert line["config"] == want
+    assert line["impl"] == "reference" and line["steps"] == 1
+    for k in ("vocab_chunk", "tiles", "cluster_multicast", "backward"):
+        assert k not in line["config"]
+    assert want["workload"].startswith("llama3_n8192") and want["N"] == 64
