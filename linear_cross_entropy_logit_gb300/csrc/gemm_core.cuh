@@ -824,8 +824,9 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
           // 64-column slices.  The epilogue runs beside the next tile's MMAs
           // and competes with them for the SM, so it is kept lean: a tile
           // wholly inside the vocabulary skips the per-column range check,
-          // the exponent argument is one FFMA, the max and sum run as four
-          // independent chains, and the target-logit gather only runs for a
+          // the exponent arguments take one packed FMA per two columns, the
+          // max and sum run as four independent chains (the sums in two
+          // packed adds), and the target-logit gather only runs for a
           // slice that holds some lane's target (a warp vote).
           const int tile_c0 = nb * BN;
           const bool full_tile = tile_c0 + BN <= p.col_limit;  // warp-uniform
@@ -868,11 +869,24 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
               ssum *= ex2_approx(m2 - cm2);
               m2 = cm2;
             }
-            float ps[4] = {0.f, 0.f, 0.f, 0.f};
+            // sum chains j mod 4, packed two per f32x2 register (each lane
+            // rounds like the scalar FMA and add: same bits)
+            uint64_t ps01 = 0ull, ps23 = 0ull;
+            const uint64_t l2e = pack_f32x2(LOG2E, LOG2E), nm2 = pack_f32x2(-m2, -m2);
 #pragma unroll
-            for (int j = 0; j < 64; ++j)
-              ps[j & 3] += ex2_approx(fmaf(__uint_as_float(r[j]), LOG2E, -m2));
-            ssum += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+            for (int j = 0; j < 64; j += 2) {
+              float a0, a1;
+              unpack_f32x2(fma_f32x2(pack_u32x2(r[j], r[j + 1]), l2e, nm2), a0, a1);
+              const uint64_t e = pack_f32x2(ex2_approx(a0), ex2_approx(a1));
+              if ((j & 3) == 0)
+                ps01 = add_f32x2(ps01, e);
+              else
+                ps23 = add_f32x2(ps23, e);
+            }
+            float p0, p1, p2, p3;
+            unpack_f32x2(ps01, p0, p1);
+            unpack_f32x2(ps23, p2, p3);
+            ssum += (p0 + p1) + (p2 + p3);
           }
         } else if constexpr (EPI == Epi::kDz) {
 #pragma unroll 1
